@@ -1,0 +1,487 @@
+#!/usr/bin/env python3
+"""Benchmark of the sink-attention hot path on GB300.
+
+Default workload (N=1): decode of 64 sequences with KV lengths uniform in
+[1024, 8192] over a paged bf16 cache (16-token pages, permuted table), 64 query
+/ 8 kv heads, head_dim 64, sinks ~ U(-2, 6); one step = the full-context call
+followed by the 128-token-window call on the same cache (the alternating
+layers of gpt-oss).  Metric: algorithmic HBM bytes / time, in GB/s.
+--config 1..5 selects the other workloads (3 = prefill, TFLOP/s).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference] [--config C]
+
+Under torchrun (N > 1) every rank runs the same per-GPU workload on its own
+GPU (independent replicas; weak scaling), the timed region is bracketed by a
+barrier and a synchronize on both sides, and rank 0 prints the max over ranks.
+`--impl reference` times the fp64 CPU oracle on a bounded sample of the same
+workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "sink-attn decode HBM GB/s (% peak); prefill TFLOP/s (% bf16 tensor peak)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+DEFAULT_STEPS = {1: 2000, 2: 2000, 3: 50, 4: 100, 5: 500}
+
+
+# ------------------------------------------------------------------ helpers
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_sha(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel_key, workload):
+    """dram bytes per launch from the committed ncu summary, if it was taken on
+    the current source of that kernel; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    e = d.get(kernel_key, {}).get(workload)
+    if not e:
+        return None
+    if e.get("source_sha") != source_sha(e.get("sources", [])):
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples around the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, device_index):
+        self.samples = []
+        self.proc = None
+        self.t0 = self.t1 = None
+        ident = None
+        try:
+            import torch
+            u = getattr(torch.cuda.get_device_properties(device_index), "uuid", None)
+            if u is not None:
+                ident = "GPU-" + str(u)
+        except Exception:
+            pass
+        cmd = ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits", "-lms", "100"]
+        if ident:
+            cmd += ["-i", ident]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.th = threading.Thread(target=self._read, daemon=True)
+        self.th.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def begin(self):
+        self.t0 = time.time()
+
+    def end(self):
+        self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        inside = [s for t, s in self.samples if self.t0 is not None and self.t0 - 0.15 <= t <= self.t1 + 0.15]
+        rows = inside or [s for _, s in self.samples]
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if len(r) > 1 and r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if len(r) > 2 and r[2].replace(".", "").isdigit()]
+        reasons = set()
+        for r in rows:
+            for i, name in enumerate(self.NAMES):
+                if len(r) > 5 + i and r[5 + i].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(rows), "in_timed_region": bool(inside)}
+
+
+# ------------------------------------------------------------ distributed
+def dist_info():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def dist_init(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend)
+    return dist
+
+
+def dist_barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def dist_max(value: float, world: int) -> float:
+    """Max of a host float over ranks (the slowest rank sets the job time)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------- workloads
+def decode_bytes(seqlens, window, hkv, hq, dim, elem_bytes, with_lse=True):
+    """Algorithmic HBM bytes of one decode call: every visible K and V element
+    once per kv head, plus q in and out (bf16) and lse (fp32)."""
+    keys = sum(min(int(L), window) if window > 0 else int(L) for L in seqlens)
+    b = len(seqlens)
+    return keys * hkv * dim * 2 * elem_bytes + 2 * b * hq * dim * 2 + (4 * b * hq if with_lse else 0)
+
+
+def prefill_flops(q_lens, kv_lens, window, hq, dim):
+    """4 * Hq * D * sum over queries of the visible keys (QK and PV)."""
+    tot = 0
+    for lq, lk in zip(q_lens, kv_lens):
+        for i in range(lq):
+            p = lk - lq + i
+            n = p + 1 if window <= 0 else min(window, p + 1)
+            tot += n
+    return 4 * hq * dim * tot
+
+
+def windows_of(cfg):
+    return {1: [0], 2: [0, 128], 3: [0, 128], 4: [0], 5: [0, 128, 0, 128]}[cfg]
+
+
+def workload_name(cfg):
+    return {
+        1: "decode B=1 L=256 contiguous bf16, 64q/8kv heads, D=64, w=0",
+        2: "decode B=64 L~U[1024,8192] paged P=16 bf16, 64q/8kv heads, D=64, step = w=0 call + w=128 call",
+        3: "prefill T=8192 causal contiguous bf16, 64q/8kv heads, D=64, step = w=0 call + w=128 call",
+        4: "decode B=128 L=32768 paged P=16 bf16 split-KV, 64q/8kv heads, D=64, w=0",
+        5: "decode B=256 L=8192 paged P=16 fp8-e4m3, 64q/8kv heads, D=64, step = w=0,128,0,128",
+    }[cfg]
+
+
+class DecodeBench:
+    """One step = the decode calls of the workload on one resident cache."""
+
+    def __init__(self, sa, cfg, device):
+        import torch
+        import workloads as W
+        self.sa, self.cfg, self.torch = sa, cfg, torch
+        gen_dev = device if cfg in (2, 4, 5) else "cpu"
+        self.case = W.make_config(cfg, window=0, device=gen_dev).to(device)
+        c = self.case
+        self.B, self.Hq, self.D = c.q.shape
+        self.Hkv = c.kv.num_kv_heads
+        self.maxlen = int(c.seqlens.max())
+        self.seqlens = [int(x) for x in c.seqlens.cpu()]
+        self.elem = 1 if c.kv.dtype == "e4m3" else 2
+        self.calls = []
+        for w in windows_of(cfg):
+            S = sa.sa_decode_num_splits(self.B, self.Hkv, self.maxlen, w)
+            out = torch.empty(self.B, self.Hq, self.D, dtype=torch.bfloat16, device=device)
+            lse = torch.empty(self.B, self.Hq, dtype=torch.float32, device=device)
+            o_part = l_part = ws = None
+            if S > 1:
+                o_part = torch.empty(S, self.B, self.Hq, self.D, dtype=torch.float32, device=device)
+                l_part = torch.empty(S, self.B, self.Hq, dtype=torch.float32, device=device)
+                nbytes = sa.sa_decode_workspace_size(self.B, self.Hq, self.Hkv, self.D, self.maxlen, w, S)
+                ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+            self.calls.append(dict(window=w, S=S, out=out, lse=lse, o_part=o_part, l_part=l_part, ws=ws,
+                                   bytes=decode_bytes(self.seqlens, w, self.Hkv, self.Hq, self.D, self.elem)))
+        self.step_bytes = sum(cl["bytes"] for cl in self.calls)
+        self.kernels_per_step = sum(2 if cl["S"] > 1 else 1 for cl in self.calls)
+        self.unit = "GB/s"
+
+    def amount(self):
+        return self.step_bytes / 1e9
+
+    def run_call(self, cl, stream, ev=None):
+        """Per call: [ev0] decode kernel [ev1] merge kernel.  For S > 1 this is
+        sa_decode_partial + sa_merge_states, the two launches sa_decode makes."""
+        sa, c = self.sa, self.case
+        if ev is not None:
+            ev[0].record(stream)
+        if cl["S"] > 1:
+            sa.sa_decode_partial(c.q, c.kv, c.seqlens, cl["window"], c.sm_scale, cl["S"], cl["o_part"],
+                                 cl["l_part"], max_kv_len=self.maxlen, stream=stream)
+            if ev is not None:
+                ev[1].record(stream)
+            sa.sa_merge_states(cl["o_part"], cl["l_part"], c.sinks, cl["out"], cl["lse"], stream=stream)
+        else:
+            sa.sa_decode(c.q, c.kv, c.seqlens, c.sinks, cl["window"], c.sm_scale, cl["out"], cl["lse"],
+                         max_kv_len=self.maxlen, num_splits=1, stream=stream)
+            if ev is not None:
+                ev[1].record(stream)
+
+    def step(self, stream, evs=None):
+        for i, cl in enumerate(self.calls):
+            self.run_call(cl, stream, None if evs is None else evs[i])
+
+    def dominant(self):
+        return 0, "decode_kernel", self.calls[0]["bytes"]
+
+    # ---- end to end through sa_decode with host buffers
+    def e2e(self, stream, steps, warmup):
+        torch = self.torch
+        c = self.case
+        hq = torch.empty(c.q.shape, dtype=c.q.dtype, pin_memory=True).copy_(c.q.cpu())
+        hs = torch.empty(c.seqlens.shape, dtype=torch.int32, pin_memory=True).copy_(c.seqlens.cpu())
+        ht = None
+        if c.kv.page_table is not None:
+            ht = torch.empty(c.kv.page_table.shape, dtype=torch.int32, pin_memory=True).copy_(c.kv.page_table.cpu())
+        houts = [(torch.empty(cl["out"].shape, dtype=torch.bfloat16, pin_memory=True),
+                  torch.empty(cl["lse"].shape, dtype=torch.float32, pin_memory=True)) for cl in self.calls]
+        h2d = hq.numel() * 2 + hs.numel() * 4 + (0 if ht is None else ht.numel() * 4)
+        d2h = sum(o.numel() * 2 + l.numel() * 4 for o, l in houts)
+
+        def one():
+            c.q.copy_(hq, non_blocking=True)
+            c.seqlens.copy_(hs, non_blocking=True)
+            if ht is not None:
+                c.kv.page_table.copy_(ht, non_blocking=True)
+            for cl, (ho, hl) in zip(self.calls, houts):
+                self.sa.sa_decode(c.q, c.kv, c.seqlens, c.sinks, cl["window"], c.sm_scale, cl["out"], cl["lse"],
+                                  max_kv_len=self.maxlen, workspace=cl["ws"], num_splits=cl["S"], stream=stream)
+                ho.copy_(cl["out"], non_blocking=True)
+                hl.copy_(cl["lse"], non_blocking=True)
+
+        with torch.cuda.stream(stream):
+            for _ in range(warmup):
+                one()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(steps):
+                one()
+            e1.record(stream)
+            torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / steps
+        return ms, h2d, d2h
+
+    # ---- oracle on a bounded sample
+    def oracle_sample(self, budget_s, max_seqs=None):
+        """(seconds per sample, bytes of the sample, description)."""
+        import oracle
+        import workloads as W
+        oracle.build()
+        c = self.case
+        n = self.B if max_seqs is None else max(1, min(self.B, max_seqs))
+        ids = list(range(n))
+        sub = W.subset(c, ids)
+        rows = oracle.decode_rows(sub.seqlens)
+        t0 = time.time()
+        nbytes = 0
+        for cl in self.calls:
+            oracle.attend(sub.q, rows[0], rows[1], sub.kv.as_dict(), sub.seqlens, sub.sinks, cl["window"],
+                          sub.sm_scale)
+            nbytes += decode_bytes([int(x) for x in sub.seqlens], cl["window"], self.Hkv, self.Hq, self.D,
+                                   self.elem)
+        dt = time.time() - t0
+        desc = "%d of %d sequences x %d heads, every call of the step (windows %s)" % (
+            n, self.B, self.Hq, [cl["window"] for cl in self.calls])
+        return dt, nbytes, desc
+
+
+# ------------------------------------------------------------------- main
+def run_native(args, world, rank, local):
+    import torch
+    import gqa_attention_sinks_head_gb300 as sa
+    sa.build()
+    sa.load()
+    torch.cuda.set_device(local)
+    dist_init(world, "nccl")
+    cfg = args.config
+    if cfg == 3:
+        raise SystemExit("prefill bench: sa_prefill is not built yet")
+    wl = DecodeBench(sa, cfg, "cuda")
+    stream = torch.cuda.Stream()
+    steps = args.steps
+    sampler = ClockSampler(local) if rank == 0 else None
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            wl.step(stream)
+    torch.cuda.synchronize()
+    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in wl.calls] for _ in range(steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    dist_barrier(world)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.begin()
+    with torch.cuda.stream(stream):
+        t_start.record(stream)
+        for i in range(steps):
+            wl.step(stream, evs[i])
+        t_end.record(stream)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.end()
+    dist_barrier(world)
+    ms = t_start.elapsed_time(t_end) / steps
+    ms = dist_max(ms, world)
+    ci, kname, kbytes = wl.dominant()
+    k_ms = statistics.fmean(evs[i][ci][0].elapsed_time(evs[i][ci][1]) for i in range(steps))
+    clocks = sampler.stop() if sampler else None
+
+    peaks, peak_src = load_peaks()
+    value = wl.amount() * world / (ms / 1e3)
+    achieved = kbytes / 1e9 / (k_ms / 1e3)
+    peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    traffic = ncu_traffic(kname, "config%d" % cfg)
+
+    e2e_ms, h2d, d2h = wl.e2e(stream, max(3, min(steps, 200)), 3)
+    e2e_value = wl.amount() * world / (e2e_ms / 1e3)
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": wl.unit, "n_gpus": world, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 6), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if wl.elem == 2 else "fp8-e4m3 kv, bf16 q/out",
+        "data": "synthetic (seeded; N(0,1) q/k/v, sinks U(-2,6)); no weights or datasets",
+        "config": {"workload": workload_name(cfg), "global_batch": wl.B * world, "seq_len_max": wl.maxlen,
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "splits": [cl["S"] for cl in wl.calls],
+                   "l2": "inputs larger than L2 (%.2f GB of KV per step); no flush" % (wl.step_bytes / 1e9)},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "kernel": kname, "algorithmic_bytes_per_launch": kbytes,
+                     "avg_launch_ms": round(k_ms, 6), "peak_source": peak_src,
+                     "frac_of_nominal_8tbs": round(achieved / 8000.0, 4)},
+        "clocks": clocks,
+        "e2e": {"value": round(e2e_value, 2), "unit": wl.unit, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "api": "sa_decode with pinned host q/seqlens/page table in, "
+                                                 "out/lse back; KV cache resident"},
+        "gpu_launches": steps * wl.kernels_per_step,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        dt, nbytes, desc = wl.oracle_sample(30.0)
+        line["cpu_baseline"] = {"value": round(nbytes / 1e9 / dt, 4), "unit": wl.unit,
+                                "cores": oracle.num_threads(), "kind": "oracle", "sample": desc,
+                                "seconds": round(dt, 2)}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_reference(args, world, rank, local):
+    """The oracle, as it stands, timed on the host cores on the native arm's
+    workload; each step is a bounded sample of it."""
+    if rank != 0:
+        return
+    import torch
+    import gqa_attention_sinks_head_gb300 as sa
+    import oracle
+    cfg = args.config
+    if cfg == 3:
+        print(json.dumps({"impl": "reference", "unavailable": "prefill oracle arm not wired yet"}))
+        return
+    oracle.build()
+    sa.build()
+    sa.load()
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+
+    class _Shim:  # the CPU arm only needs the split count for the byte formula
+        def __init__(self):
+            self.inner = sa
+
+        def __getattr__(self, k):
+            return getattr(self.inner, k)
+
+    wl = DecodeBench(_Shim(), cfg, dev)
+    total_budget = 120.0
+    steps, warmup = args.steps, args.warmup
+    # size the per-step sample from a one-sequence pilot
+    dt1, b1, _ = wl.oracle_sample(5.0, max_seqs=1)
+    per_step = total_budget / max(1, steps + warmup)
+    n = max(1, min(wl.B, int(per_step / max(dt1, 1e-6))))
+    for _ in range(warmup):
+        wl.oracle_sample(per_step, max_seqs=n)
+    t0 = time.time()
+    nbytes = 0
+    desc = ""
+    for _ in range(steps):
+        _, nb, desc = wl.oracle_sample(per_step, max_seqs=n)
+        nbytes += nb
+    dt = time.time() - t0
+    value = nbytes / 1e9 / dt
+    line = {
+        "metric": METRIC, "value": round(value, 4), "unit": wl.unit, "n_gpus": world, "steps": steps,
+        "warmup": warmup, "ms_per_step": round(dt / steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded), same bytes as the native arm",
+        "config": {"workload": workload_name(cfg), "global_batch": wl.B, "seq_len_max": wl.maxlen},
+        "impl": "reference",
+        "cpu_baseline": {"value": round(value, 4), "unit": wl.unit, "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": desc},
+        "e2e": {"value": round(value, 4), "unit": wl.unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.steps is None:
+        args.steps = DEFAULT_STEPS[args.config]
+    args.warmup = max(3, args.warmup)
+    world, rank, local = dist_info()
+    if args.impl == "reference":
+        run_reference(args, world, rank, local)
+    else:
+        run_native(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

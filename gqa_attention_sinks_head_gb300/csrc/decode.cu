@@ -1,0 +1,463 @@
+// decode.cu -- paged-KV sink-attention decode for sm_103a.
+//
+// One thread block per (KV chunk, kv head g, sequence b).  The G <= 8 query
+// heads of kv head g share every K/V byte the block reads: the scores of a
+// 16-key tile are one tensor-core product S^T = K . Q^T (keys on the mma M
+// dimension, the group's heads on N = 8), and the value update is a second
+// product O^T += V^T . P^T, so no head re-reads the cache and the fp32 math
+// never runs on the FMA pipe at a rate the HBM stream cannot hide.
+//
+// Pipeline: warp 4 is the producer.  It walks the page table (32 entries
+// prefetched ahead in registers) and issues one TMA tile copy per 16-key page
+// slice of K and of V (2 KB each in bf16, 1 KB in FP8) into a 4-stage ring,
+// completing on an mbarrier with transaction bytes.  Warps 0-3 are consumers:
+// stage i holds four tiles, one per consumer warp.  The tiles land in shared
+// memory with the TMA 128-byte (bf16) / 64-byte (FP8) swizzle so that the
+// ldmatrix reads below are free of bank conflicts.
+//
+// Per tile and consumer warp: ldmatrix K -> 4 (bf16) mma for S^T; online
+// softmax in base 2 (max via 3 warp shuffles per head pair); P packed to
+// 16-bit and transposed in registers with movmatrix into the B operand of the
+// value product; ldmatrix.trans V -> 4 mma for O^T.  The softmax follows
+// "GPT-OSS on day 0" (Perplexity), section "Sink Attention": a running max m
+// and a scale sum d per head, with m started at the head's sink and d at 1
+// -- in warp 0 of the unsplit call only, so that the sink is counted once;
+// every other warp (and every chunk of a split call) starts from m = -inf,
+// d = 0.  At the end the block merges its four warp states through shared
+// memory and writes either the final output (bf16 + natural-log lse) or a
+// sink-free partial state for sa_merge_states.
+//
+// FP8-E4M3 caches (vLLM "GPT-OSS optimisations on NVIDIA Blackwell", FP8 KV
+// cache) are widened in registers to f16 holding code * 2^-8 (exact for every
+// code, see e4m3x2_to_f16x2_scaled), the products run as f16 mma, and
+// 2^8 * k_scale (resp. 2^8 * v_scale) is folded into the score scale (resp.
+// the output scale).  Q is rounded to f16 for that path.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "sa_internal.h"
+#include "sa_ptx.cuh"
+
+namespace sa {
+namespace {
+
+constexpr int kConsumerWarps = 4;
+constexpr int kStages = 4;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr float kLn2 = 0.69314718055994530942f;
+constexpr float kLog2e = 1.44269504088896340736f;
+
+template <bool FP8>
+struct DecodeCfg {
+    static constexpr int kRowBytes = kHeadDim * (FP8 ? 1 : 2);  // 64 or 128
+    static constexpr int kTileBytes = kTile * kRowBytes;        // 1 KB or 2 KB
+};
+
+template <bool FP8>
+struct DecodeSmem {
+    // K and V tiles of each stage, one per consumer warp (1 KB aligned).
+    uint8_t k[kStages][kConsumerWarps][DecodeCfg<FP8>::kTileBytes];
+    uint8_t v[kStages][kConsumerWarps][DecodeCfg<FP8>::kTileBytes];
+    float red_m[kConsumerWarps][kMaxGroup];
+    float red_l[kConsumerWarps][kMaxGroup];
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+};
+// The per-warp O^T partials of the final merge reuse the K tiles.
+static_assert(sizeof(float) * kConsumerWarps * kHeadDim * kMaxGroup <=
+                  sizeof(uint8_t) * kStages * kConsumerWarps * DecodeCfg<true>::kTileBytes,
+              "merge scratch must fit in the K tiles");
+
+// Byte offset of 16-byte chunk `chunk` of row `row` in a swizzled tile.
+template <bool FP8>
+__device__ __forceinline__ uint32_t swz(int row, int chunk)
+{
+    if constexpr (FP8)  // 64-byte rows, 64B swizzle: chunk ^= (row / 2) % 4
+        return row * 64 + ((chunk ^ ((row >> 1) & 3)) << 4);
+    else  // 128-byte rows, 128B swizzle: chunk ^= row % 8
+        return row * 128 + ((chunk ^ (row & 7)) << 4);
+}
+
+template <bool FP8>
+__global__ void __launch_bounds__(kThreads, 3) decode_kernel(const __grid_constant__ CUtensorMap tmk,
+                                                             const __grid_constant__ CUtensorMap tmv,
+                                                             const DecodeParams p)
+{
+    using Cfg = DecodeCfg<FP8>;
+    extern __shared__ uint8_t smem_raw[];
+    DecodeSmem<FP8> &sm =
+        *reinterpret_cast<DecodeSmem<FP8> *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int split = blockIdx.x;
+    const int g = blockIdx.y;
+    const int b = blockIdx.z;
+
+    // ---- the block's key range ------------------------------------------
+    int L = __ldg(p.seqlens + b);
+    if (L < 0 || L > p.max_kv_len) {
+        if (threadIdx.x == 0)
+            atomicOr(p.status, SA_DEVICE_SEQLEN_RANGE);
+        L = min(max(L, 0), p.max_kv_len);
+    }
+    const int lo = p.window > 0 ? max(0, L - p.window) : 0;       // first visible key
+    const int t_begin = (lo & ~(kTile - 1)) + kTile * p.tiles_per_split * split;  // tile-aligned
+    const int t_first = max(t_begin, lo);
+    const int t_end = min(L, t_begin + kTile * p.tiles_per_split);
+    const int ntiles = t_end > t_first ? (t_end - t_begin + kTile - 1) / kTile : 0;
+    const int nstages = (ntiles + kConsumerWarps - 1) / kConsumerWarps;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&sm.full[i], 1);
+            mbar_init(&sm.empty[i], kConsumerWarps);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    // consumer state, kept past the role split for the block-level merge
+    float m[2] = {-INFINITY, -INFINITY};
+    float l[2] = {0.f, 0.f};
+    float o[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            o[i][j] = 0.f;
+    const int r = lane >> 2;  // mma row group: key r / r+8 of a tile; head r in the B operand
+    const int c = lane & 3;   // mma column pair: heads 2c, 2c+1 of the accumulators
+
+    if (warp == kConsumerWarps) {
+        // =================== producer: page-table walk + TMA ================
+        if (lane == 0) {
+            tma_prefetch_desc(&tmk);
+            tma_prefetch_desc(&tmv);
+        }
+        const int32_t *trow = p.page_table ? p.page_table + static_cast<int64_t>(b) * p.table_stride : nullptr;
+        auto page_of = [&](int tile) -> int {
+            if (tile >= ntiles)
+                return 0;
+            if (!trow)
+                return b;
+            return __ldg(trow + (t_begin + tile * kTile) / p.page_size);
+        };
+        int pg_cur = page_of(lane);        // lane j: page of tile 32k + j
+        int pg_next = page_of(32 + lane);  // the next 32, one batch ahead
+        const uint64_t pol = l2_policy_evict_first();
+        for (int st = 0; st < nstages; ++st) {
+            const int buf = st % kStages;
+            const int tile0 = st * kConsumerWarps;
+            if (tile0 > 0 && (tile0 & 31) == 0) {
+                pg_cur = pg_next;
+                pg_next = page_of(tile0 + 32 + lane);
+            }
+            const int page = __shfl_sync(0xffffffffu, pg_cur, (tile0 & 31) + (lane & (kConsumerWarps - 1)));
+            if (st >= kStages && !mbar_wait(&sm.empty[buf], ((st / kStages) - 1) & 1, p.status))
+                break;
+            const int nt = min(kConsumerWarps, ntiles - tile0);
+            if (lane == 0)
+                mbar_arrive_expect_tx(&sm.full[buf], static_cast<uint32_t>(nt * 2 * Cfg::kTileBytes));
+            __syncwarp();
+            if (lane < nt) {
+                if (page < 0 || page >= p.num_pages)
+                    atomicOr(p.status, SA_DEVICE_BAD_PAGE);  // the TMA box falls outside: zeros
+                const int slot = (t_begin + (tile0 + lane) * kTile) % p.page_size;
+                // coordinates in the tensor map's dimension order (dim 0 = head_dim)
+                const int c1 = p.dim_token == 1 ? slot : (p.dim_head == 1 ? g : page);
+                const int c2 = p.dim_token == 2 ? slot : (p.dim_head == 2 ? g : page);
+                const int c3 = p.dim_token == 3 ? slot : (p.dim_head == 3 ? g : page);
+                tma_load_4d_hint(sm.k[buf][lane], &tmk, &sm.full[buf], 0, c1, c2, c3, pol);
+                tma_load_4d_hint(sm.v[buf][lane], &tmv, &sm.full[buf], 0, c1, c2, c3, pol);
+            }
+        }
+    } else {
+        // =================== consumers ======================================
+        const int h0 = g * p.group;
+
+        // Q^T as the B operand (K dimension = head_dim, N = the group's heads).
+        uint32_t qf[4][2];
+        {
+            const __nv_bfloat16 *qrow = reinterpret_cast<const __nv_bfloat16 *>(p.q) +
+                                        (static_cast<int64_t>(b) * p.num_qo_heads + h0 + r) * kHeadDim;
+            const bool ok = r < p.group;
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+                if constexpr (FP8) {
+                    // k-step ks pairs (4c, 4c+1) and (4c+2, 4c+3) of the 16-dim block,
+                    // the order in which the E4M3 K bytes arrive (see below).
+                    uint2 w = ok ? *reinterpret_cast<const uint2 *>(qrow + 16 * ks + 4 * c) : make_uint2(0, 0);
+                    __nv_bfloat162 x01 = *reinterpret_cast<__nv_bfloat162 *>(&w.x);
+                    __nv_bfloat162 x23 = *reinterpret_cast<__nv_bfloat162 *>(&w.y);
+                    qf[ks][0] = pack_f16(__bfloat162float(x01.x), __bfloat162float(x01.y));
+                    qf[ks][1] = pack_f16(__bfloat162float(x23.x), __bfloat162float(x23.y));
+                } else {
+                    qf[ks][0] = ok ? *reinterpret_cast<const uint32_t *>(qrow + 16 * ks + 2 * c) : 0u;
+                    qf[ks][1] = ok ? *reinterpret_cast<const uint32_t *>(qrow + 16 * ks + 2 * c + 8) : 0u;
+                }
+            }
+        }
+
+        // Running state for heads 2c, 2c+1 (m in base 2; l a per-lane partial sum).
+        if (!p.partial && warp == 0 && p.sinks) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int n = 2 * c + j;
+                if (n < p.group) {
+                    m[j] = __ldg(p.sinks + h0 + n) * kLog2e;  // m starts at the sink ...
+                    l[j] = (r == 0) ? 1.f : 0.f;              // ... and d at 1 (counted once)
+                }
+            }
+        }
+        const int lr = lane & 7;
+        const int mi = lane >> 3;
+        for (int st = 0; st < nstages; ++st) {
+            const int buf = st % kStages;
+            if (!mbar_wait(&sm.full[buf], (st / kStages) & 1, p.status))
+                break;
+            const int tile = st * kConsumerWarps + warp;
+            if (tile < ntiles) {
+                const int tok0 = t_begin + tile * kTile;
+                const uint32_t kt = smem_u32(sm.k[buf][warp]);
+                const uint32_t vt = smem_u32(sm.v[buf][warp]);
+
+                // ---- S^T = K . Q^T  (16 keys x 8 heads, fp32) --------------
+                float s[4] = {0.f, 0.f, 0.f, 0.f};
+                if constexpr (FP8) {
+#pragma unroll
+                    for (int j2 = 0; j2 < 2; ++j2) {
+                        uint32_t R0, R1, R2, R3;
+                        ldsm_x4(kt + swz<true>((mi & 1) * 8 + lr, 2 * j2 + (mi >> 1)), R0, R1, R2, R3);
+                        mma_f16(s, e4m3x2_to_f16x2_scaled<kSel01>(R0), e4m3x2_to_f16x2_scaled<kSel01>(R1),
+                                e4m3x2_to_f16x2_scaled<kSel23>(R0), e4m3x2_to_f16x2_scaled<kSel23>(R1),
+                                qf[2 * j2][0], qf[2 * j2][1]);
+                        mma_f16(s, e4m3x2_to_f16x2_scaled<kSel01>(R2), e4m3x2_to_f16x2_scaled<kSel01>(R3),
+                                e4m3x2_to_f16x2_scaled<kSel23>(R2), e4m3x2_to_f16x2_scaled<kSel23>(R3),
+                                qf[2 * j2 + 1][0], qf[2 * j2 + 1][1]);
+                    }
+                } else {
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks) {
+                        uint32_t a0, a1, a2, a3;
+                        ldsm_x4(kt + swz<false>((mi & 1) * 8 + lr, 2 * ks + (mi >> 1)), a0, a1, a2, a3);
+                        mma_bf16(s, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+                    }
+                }
+
+                // ---- online softmax (base 2) -------------------------------
+                // s[0]: key r, head 2c   s[1]: key r, head 2c+1
+                // s[2]: key r+8, head 2c s[3]: key r+8, head 2c+1
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    s[i] *= p.score_scale;
+                const bool edge = tok0 < t_first || tok0 + kTile > t_end;
+                uint32_t vm01 = 0xffffffffu, vm23 = 0xffffffffu;
+                if (edge) {
+                    const bool v0 = tok0 + r >= t_first && tok0 + r < t_end;
+                    const bool v8 = tok0 + r + 8 >= t_first && tok0 + r + 8 < t_end;
+                    s[0] = v0 ? s[0] : -INFINITY;
+                    s[1] = v0 ? s[1] : -INFINITY;
+                    s[2] = v8 ? s[2] : -INFINITY;
+                    s[3] = v8 ? s[3] : -INFINITY;
+                    // value rows outside the range are zeroed (a NaN there must not leak via 0 * NaN)
+                    const int k0 = tok0 + 2 * c, k8 = tok0 + 2 * c + 8;
+                    vm01 = ((k0 >= t_first && k0 < t_end) ? 0x0000ffffu : 0u) |
+                           ((k0 + 1 >= t_first && k0 + 1 < t_end) ? 0xffff0000u : 0u);
+                    vm23 = ((k8 >= t_first && k8 < t_end) ? 0x0000ffffu : 0u) |
+                           ((k8 + 1 >= t_first && k8 + 1 < t_end) ? 0xffff0000u : 0u);
+                }
+                float mx0 = fmaxf(s[0], s[2]);
+                float mx1 = fmaxf(s[1], s[3]);
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1) {
+                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+                }
+                const float mn0 = fmaxf(m[0], mx0);
+                const float mn1 = fmaxf(m[1], mx1);
+                const float mu0 = mn0 == -INFINITY ? 0.f : mn0;  // nothing seen yet: keep exp2 finite
+                const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
+                const float al0 = ex2(m[0] - mu0);
+                const float al1 = ex2(m[1] - mu1);
+                const float p0 = ex2(s[0] - mu0);
+                const float p1 = ex2(s[1] - mu1);
+                const float p2 = ex2(s[2] - mu0);
+                const float p3 = ex2(s[3] - mu1);
+                l[0] = l[0] * al0 + (p0 + p2);
+                l[1] = l[1] * al1 + (p1 + p3);
+                m[0] = mn0;
+                m[1] = mn1;
+#pragma unroll
+                for (int mt = 0; mt < 4; ++mt) {
+                    o[mt][0] *= al0;
+                    o[mt][1] *= al1;
+                    o[mt][2] *= al0;
+                    o[mt][3] *= al1;
+                }
+                // P (key-major C layout) -> P^T as the B operand (K = keys, N = heads)
+                uint32_t pb0, pb1;
+                if constexpr (FP8) {
+                    pb0 = movmatrix_t(pack_f16(p0, p1));
+                    pb1 = movmatrix_t(pack_f16(p2, p3));
+                } else {
+                    pb0 = movmatrix_t(pack_bf16(p0, p1));
+                    pb1 = movmatrix_t(pack_bf16(p2, p3));
+                }
+
+                // ---- O^T += V^T . P^T ---------------------------------------
+                if constexpr (FP8) {
+#pragma unroll
+                    for (int j2 = 0; j2 < 2; ++j2) {
+                        uint32_t R0, R1, R2, R3;
+                        ldsm_x4_t(vt + swz<true>((mi & 1) * 8 + lr, 2 * j2 + (mi >> 1)), R0, R1, R2, R3);
+                        // rows of m-tile 2*j2 (+1): row r <-> dim 16ch + 2r, row r+8 <-> 16ch + 2r + 1
+                        mma_f16(o[2 * j2], e4m3x2_to_f16x2_scaled<kSel02>(R0) & vm01,
+                                e4m3x2_to_f16x2_scaled<kSel13>(R0) & vm01, e4m3x2_to_f16x2_scaled<kSel02>(R1) & vm23,
+                                e4m3x2_to_f16x2_scaled<kSel13>(R1) & vm23, pb0, pb1);
+                        mma_f16(o[2 * j2 + 1], e4m3x2_to_f16x2_scaled<kSel02>(R2) & vm01,
+                                e4m3x2_to_f16x2_scaled<kSel13>(R2) & vm01, e4m3x2_to_f16x2_scaled<kSel02>(R3) & vm23,
+                                e4m3x2_to_f16x2_scaled<kSel13>(R3) & vm23, pb0, pb1);
+                    }
+                } else {
+#pragma unroll
+                    for (int mt = 0; mt < 4; ++mt) {
+                        uint32_t a0, a1, a2, a3;
+                        ldsm_x4_t(vt + swz<false>((mi >> 1) * 8 + lr, 2 * mt + (mi & 1)), a0, a1, a2, a3);
+                        mma_bf16(o[mt], a0 & vm01, a1 & vm01, a2 & vm23, a3 & vm23, pb0, pb1);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&sm.empty[buf]);
+        }
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            l[j] += __shfl_xor_sync(0xffffffffu, l[j], 4);
+            l[j] += __shfl_xor_sync(0xffffffffu, l[j], 8);
+            l[j] += __shfl_xor_sync(0xffffffffu, l[j], 16);
+        }
+    }
+    __syncthreads();  // every warp is done with the tiles: their K area holds the merge scratch
+    float *red_o = reinterpret_cast<float *>(&sm.k[0][0][0]);  // [warp][dim][head]
+    if (warp < kConsumerWarps) {
+        if (r == 0) {
+            sm.red_m[warp][2 * c] = m[0];
+            sm.red_m[warp][2 * c + 1] = m[1];
+            sm.red_l[warp][2 * c] = l[0];
+            sm.red_l[warp][2 * c + 1] = l[1];
+        }
+        float *w = red_o + warp * kHeadDim * kMaxGroup;
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt) {
+            const int dlo = FP8 ? 16 * mt + 2 * r : 16 * mt + r;
+            const int dhi = FP8 ? dlo + 1 : dlo + 8;
+            w[dlo * kMaxGroup + 2 * c] = o[mt][0];
+            w[dlo * kMaxGroup + 2 * c + 1] = o[mt][1];
+            w[dhi * kMaxGroup + 2 * c] = o[mt][2];
+            w[dhi * kMaxGroup + 2 * c + 1] = o[mt][3];
+        }
+    }
+    __syncthreads();
+
+    // ---- merge the four warp states; thread t: head t/16, dims 4*(t%16).. ----
+    if (threadIdx.x < 128) {
+        const int n = threadIdx.x >> 4;
+        const int d0 = (threadIdx.x & 15) * 4;
+        if (n < p.group) {
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w)
+                M = fmaxf(M, sm.red_m[w][n]);
+            float Ls = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
+            if (M != -INFINITY) {
+#pragma unroll
+                for (int w = 0; w < kConsumerWarps; ++w) {
+                    const float sc = ex2(sm.red_m[w][n] - M);
+                    Ls += sc * sm.red_l[w][n];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        acc[i] += sc * red_o[(w * kHeadDim + d0 + i) * kMaxGroup + n];
+                }
+            }
+            const float inv = Ls > 0.f ? p.out_scale / Ls : 0.f;
+            const float lse = Ls > 0.f ? (M + lg2(Ls)) * kLn2 : -INFINITY;
+            const int h = g * p.group + n;
+            if (p.partial) {
+                const int64_t row = (static_cast<int64_t>(split) * p.batch + b) * p.num_qo_heads + h;
+                *reinterpret_cast<float4 *>(p.o_part + row * kHeadDim + d0) =
+                    make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
+                if (d0 == 0)
+                    p.lse_part[row] = lse;
+            } else {
+                const int64_t row = static_cast<int64_t>(b) * p.num_qo_heads + h;
+                uint2 pk;
+                pk.x = pack_bf16(acc[0] * inv, acc[1] * inv);
+                pk.y = pack_bf16(acc[2] * inv, acc[3] * inv);
+                *reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(p.out) + row * kHeadDim + d0) = pk;
+                if (d0 == 0 && p.lse)
+                    p.lse[row] = lse;
+            }
+        }
+    }
+}
+
+template <bool FP8>
+size_t decode_smem_bytes()
+{
+    return sizeof(DecodeSmem<FP8>) + 1024;  // + slack for the 1 KB alignment
+}
+
+template <bool FP8>
+cudaError_t prepare_decode()
+{
+    // one cudaFuncSetAttribute per device and variant
+    static int done[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev >= 0 && dev < 64 && done[dev])
+        return cudaSuccess;
+    e = cudaFuncSetAttribute(decode_kernel<FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(decode_smem_bytes<FP8>()));
+    if (e == cudaSuccess && dev >= 0 && dev < 64)
+        done[dev] = 1;
+    return e;
+}
+
+}  // namespace
+
+cudaError_t decode_occupancy(bool fp8, int *blocks_per_sm)
+{
+    cudaError_t e = fp8 ? prepare_decode<true>() : prepare_decode<false>();
+    if (e != cudaSuccess)
+        return e;
+    if (fp8)
+        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, decode_kernel<true>, kThreads,
+                                                             decode_smem_bytes<true>());
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, decode_kernel<false>, kThreads,
+                                                         decode_smem_bytes<false>());
+}
+
+cudaError_t launch_decode(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p, bool fp8,
+                          cudaStream_t stream)
+{
+    const dim3 grid(p.num_splits, p.num_kv_heads, p.batch);
+    cudaError_t e;
+    if (fp8) {
+        e = prepare_decode<true>();
+        if (e != cudaSuccess)
+            return e;
+        decode_kernel<true><<<grid, kThreads, decode_smem_bytes<true>(), stream>>>(tk, tv, p);
+    } else {
+        e = prepare_decode<false>();
+        if (e != cudaSuccess)
+            return e;
+        decode_kernel<false><<<grid, kThreads, decode_smem_bytes<false>(), stream>>>(tk, tv, p);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace sa

@@ -1,0 +1,67 @@
+// sa_internal.h -- host-side structures shared by the C ABI (api.cu) and the
+// kernel launchers (decode.cu, merge.cu, prefill.cu).  Not part of the ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime_api.h>
+#include <stdint.h>
+
+namespace sa {
+
+constexpr int kHeadDim = 64;   // the kernels handle head_dim 64 only
+constexpr int kTile = 16;      // decode: keys per tile (one mma M dimension)
+constexpr int kMaxGroup = 8;   // decode: query heads per kv head (mma N = 8)
+
+// Decode launch description (one call of sa_decode / sa_decode_partial).
+struct DecodeParams {
+    const void *q;             // bf16 [B, Hq, 64]
+    const int32_t *seqlens;    // [B]
+    const int32_t *page_table; // [B, table_stride] or nullptr
+    const float *sinks;        // [Hq] or nullptr (final mode only)
+    void *out;                 // final: bf16 [B, Hq, 64]
+    float *lse;                // final: [B, Hq] or nullptr
+    float *o_part;             // partial: [S, B, Hq, 64]
+    float *lse_part;           // partial: [S, B, Hq]
+    uint32_t *status;          // device status word
+    int32_t batch, num_qo_heads, num_kv_heads, group;
+    int32_t page_size, table_stride, num_pages, max_kv_len;
+    int32_t window, num_splits, tiles_per_split;
+    int32_t partial;           // 1: write sink-free partial states; 0: final output
+    int32_t dim_token, dim_head, dim_page;  // tensor-map dimension (1..3) of each coordinate
+    float score_scale;         // multiplies q.k to give base-2 logits
+    float out_scale;           // multiplies the normalised value sum (FP8: v_scale * 2^8)
+};
+
+struct MergeParams {
+    const float *o_part;
+    const float *lse_part;
+    const float *sinks;
+    void *out;
+    float *lse_out;
+    int32_t num_splits, n, num_heads, head_dim;
+};
+
+// Prefill launch description.
+struct PrefillParams {
+    const int32_t *cu_seqlens_q;  // [B+1]
+    const int32_t *seqlens_kv;    // [B]
+    const int32_t *page_table;    // [B, table_stride] or nullptr
+    const float *sinks;
+    void *out;                    // bf16 [Tq, Hq, 64]
+    float *lse;                   // [Tq, Hq] or nullptr
+    uint32_t *status;
+    int32_t batch, num_qo_heads, num_kv_heads, group;
+    int32_t page_size, table_stride, num_pages, max_q_len, max_kv_len;
+    int32_t window, num_q_tiles;
+    float score_scale;            // sm_scale * log2(e)
+};
+
+// Launchers (return the launch error, if any).
+cudaError_t launch_decode(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p,
+                          bool fp8, cudaStream_t stream);
+cudaError_t decode_occupancy(bool fp8, int *blocks_per_sm);
+cudaError_t launch_merge(const MergeParams &p, cudaStream_t stream);
+cudaError_t launch_prefill(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                           const PrefillParams &p, cudaStream_t stream);
+
+}  // namespace sa

@@ -1,0 +1,246 @@
+/*
+ * sink_attn.h -- C ABI of libsinkattn, grouped-query attention with per-head
+ * attention sinks (the gpt-oss attention layer) on NVIDIA GB300 (sm_103a).
+ *
+ * The operation.  For a query row at position p of sequence b and query head
+ * h, with G = num_qo_heads / num_kv_heads and kv head g = floor(h / G):
+ *
+ *   J     = { j : 0 <= j <= p, j < L_b, and (window == 0 or j > p - window) }
+ *   s_j   = sm_scale * <q[h], k[b, g, j]>
+ *   sigma = sinks[h]  (-inf when sinks == NULL)
+ *   out   = sum_{j in J} exp(s_j - M) v[b, g, j] / (exp(sigma - M) + sum_{j in J} exp(s_j - M))
+ *   lse   = M + log(exp(sigma - M) + sum_{j in J} exp(s_j - M)),   M = max(sigma, max_J s_j)
+ *
+ * i.e. a softmax over the scores plus one extra per-head logit, the sink,
+ * which takes part in the denominator and has no value vector.  A row with no
+ * visible key gets out = 0 and lse = sigma.  lse is a natural logarithm and
+ * includes the sink.
+ *
+ * Sources: "GPT-OSS on day 0" (Perplexity), section "Attention: GQA with
+ * attention sinks" (one pretrained sink parameter per attention head that
+ * joins the softmax) and section "GPT-OSS kernels / Sink Attention" (the sink
+ * is an extra bias term beside the Q.K products; the online softmax seeds its
+ * running max with the sink, and a sequence split counts the sink in one chunk
+ * only).  NVIDIA gpt-oss launch article, introduction: layers alternate full
+ * causal context and a 128-token sliding window (window = 128 here means the
+ * keys j in (p - 128, p]).  vLLM "GPT-OSS optimisations on NVIDIA Blackwell",
+ * section "FlashInfer integration": an FP8 KV cache.
+ *
+ * Conventions shared by every call.
+ *  - Memory: every pointer argument is caller-owned.  Device pointers must stay
+ *    valid until the work queued on `stream` has finished.  The library
+ *    allocates no device memory per call; scratch for split-KV lives in a
+ *    caller-given workspace.
+ *  - Asynchrony: every call only queues kernels on `stream` and returns; none
+ *    synchronises the host.  Results are ready when the stream's work is done.
+ *  - Errors: argument errors are detected on the host before any launch and
+ *    return SA_ERR_INVALID_ARG (malformed) or SA_ERR_UNSUPPORTED (well formed
+ *    but outside what the kernels handle); nothing is launched then.  A failed
+ *    launch returns SA_ERR_CUDA.  sa_last_error() gives a one-line message for
+ *    the calling thread's most recent failure.  Conditions that only the
+ *    device can see (a sequence longer than max_kv_len, a page index outside
+ *    the pool, a pipeline wait that ran out its time limit) are recorded in a
+ *    device status word that sa_device_status() reads; the kernels never trap.
+ *  - Layouts: all tensors are dense with the innermost dimension contiguous
+ *    unless a stride argument says otherwise.  head_dim must be 64.
+ *  - Threads: the calls are re-entrant; concurrent calls on different streams
+ *    are independent.
+ */
+#ifndef SINK_ATTN_H
+#define SINK_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SA_VERSION 10000 /* 1.0.0 */
+
+typedef enum {
+    SA_OK = 0,
+    SA_ERR_INVALID_ARG = 1, /* malformed argument; nothing launched */
+    SA_ERR_UNSUPPORTED = 2, /* valid but not handled (head_dim != 64, ...); nothing launched */
+    SA_ERR_WORKSPACE = 3,   /* workspace missing or smaller than sa_decode_workspace_size() */
+    SA_ERR_CUDA = 4,        /* a CUDA call or launch failed; see sa_last_error() */
+    SA_ERR_TIMEOUT = 5      /* (sa_device_status only) a device wait ran out its limit */
+} sa_status_t;
+
+typedef enum {
+    SA_KV_BF16 = 0,     /* bfloat16 K and V */
+    SA_KV_FP8_E4M3 = 1  /* OCP FP8 E4M3 codes; real value = code * k_scale (resp. v_scale) */
+} sa_kv_dtype_t;
+
+/*
+ * A paged KV cache.  Token t of sequence b, kv head g, lives in page
+ *   page = page_table[b * page_table_stride + t / page_size]   (page_table != NULL)
+ *   page = b                                                   (page_table == NULL)
+ * at element offset  page * stride_page + g * stride_head + (t % page_size) * stride_token
+ * of `k` (resp. `v`); the head_dim elements of one token are contiguous.
+ * HND pages ([num_pages, num_kv_heads, page_size, head_dim]) and NHD pages
+ * ([num_pages, page_size, num_kv_heads, head_dim]) are both expressible.
+ * Requirements: k and v 16-byte aligned; every stride times the element size
+ * a multiple of 16 bytes; page_size a multiple of 16; head_dim == 64.
+ * The page table is int32 in device memory, one row of page_table_stride
+ * entries per sequence, and must hold ceil(max_kv_len / page_size) entries per
+ * row.  A page index outside [0, num_pages) is not read: the kernels load
+ * zeros for it and set SA_DEVICE_BAD_PAGE in the device status word.
+ */
+typedef struct {
+    const void *k;
+    const void *v;
+    int32_t dtype;            /* sa_kv_dtype_t */
+    int32_t num_pages;
+    int32_t num_kv_heads;
+    int32_t head_dim;
+    int32_t page_size;
+    int32_t page_table_stride;
+    int64_t stride_page;      /* elements */
+    int64_t stride_head;      /* elements */
+    int64_t stride_token;     /* elements */
+    const int32_t *page_table;
+    float k_scale;            /* FP8 only: real = code * k_scale; ignored for bf16 */
+    float v_scale;            /* FP8 only */
+} sa_kv_desc_t;
+
+/* Bits of the device status word (sa_device_status). */
+#define SA_DEVICE_SEQLEN_RANGE 0x1u /* a seqlen was < 0 or > max_kv_len: clamped */
+#define SA_DEVICE_BAD_PAGE 0x2u     /* a page index outside [0, num_pages): read as zeros */
+#define SA_DEVICE_TIMEOUT 0x4u      /* a pipeline wait ran out its limit: output undefined */
+#define SA_DEVICE_BAD_QLEN 0x8u     /* prefill: a query length was < 0 or > L_kv or > max_q_len */
+
+/*
+ * sa_decode -- one query token per sequence against its paged KV cache.
+ * Source: "GPT-OSS on day 0", sections "Sink Attention" (the online softmax
+ * seeded with the sink; parallel over heads and KV length) and the NVIDIA
+ * launch article's introduction (window).
+ *
+ *   q          device bf16 [batch, num_qo_heads, 64]; row b is sequence b's query,
+ *              at position seqlens[b] - 1 (its own key is already in the cache)
+ *   kv         KV cache descriptor (host struct, read during the call only)
+ *   seqlens    device int32 [batch]: keys held by each sequence (0 allowed)
+ *   batch      >= 0 (0: no-op)
+ *   num_qo_heads  multiple of kv->num_kv_heads, at most 8 query heads per kv head
+ *   max_kv_len host upper bound on seqlens[]; sizes the work split.  A larger
+ *              seqlen is clamped on the device and flagged.
+ *   sinks      device fp32 [num_qo_heads] (natural-log units, not scaled by
+ *              sm_scale), or NULL for no sink
+ *   window     0 = full causal; w > 0 = the w most recent keys
+ *   sm_scale   softmax scale applied to q.k (finite)
+ *   out        device bf16 [batch, num_qo_heads, 64] (round to nearest even)
+ *   lse        device fp32 [batch, num_qo_heads] or NULL
+ *   workspace  device scratch of at least sa_decode_workspace_size(...) bytes,
+ *              16-byte aligned; may be NULL when that size is 0
+ *   num_splits 0 = choose automatically (sa_decode_num_splits); 1 = no split;
+ *              S > 1 = cut every sequence's visible keys into S chunks whose
+ *              partial states are merged (sink once) by a second kernel
+ *   stream     CUDA stream (0 = legacy default stream)
+ * Returns SA_OK, SA_ERR_INVALID_ARG, SA_ERR_UNSUPPORTED, SA_ERR_WORKSPACE or SA_ERR_CUDA.
+ */
+sa_status_t sa_decode(const void *q, const sa_kv_desc_t *kv, const int32_t *seqlens,
+                      int32_t batch, int32_t num_qo_heads, int32_t max_kv_len,
+                      const float *sinks, int32_t window, float sm_scale,
+                      void *out, float *lse, void *workspace, size_t workspace_bytes,
+                      int32_t num_splits, cudaStream_t stream);
+
+/*
+ * Number of KV chunks sa_decode uses for num_splits = 0 on the current device.
+ * Depends only on the arguments and the device's SM count (no device sync).
+ */
+int32_t sa_decode_num_splits(int32_t batch, int32_t num_kv_heads, int32_t max_kv_len,
+                             int32_t window);
+
+/*
+ * Workspace bytes sa_decode needs.  num_splits = 0 gives the size for the
+ * automatic choice (num_kv_heads is needed for it); 1 gives 0.
+ * Layout when S > 1: fp32 o_part [S, batch, num_qo_heads, head_dim] followed
+ * (at a 256-byte aligned offset) by fp32 lse_part [S, batch, num_qo_heads].
+ */
+size_t sa_decode_workspace_size(int32_t batch, int32_t num_qo_heads, int32_t num_kv_heads,
+                                int32_t head_dim, int32_t max_kv_len, int32_t window,
+                                int32_t num_splits);
+
+/*
+ * sa_decode_partial -- the first half of a split decode, exposed for callers
+ * that merge partial states themselves (for example states gathered from
+ * several devices that each hold part of a sequence's keys).
+ * Chunking: for sequence b the visible keys are [lo, L_b) with
+ * lo = max(0, L_b - window) (window > 0) or 0; with a = lo rounded down to a
+ * multiple of 16 and T = ceil(tiles / num_splits) 16-key tiles per chunk
+ * (tiles = ceil(max_kv_len / 16), or ceil((min(window, max_kv_len) + 15) / 16)
+ * when window > 0), chunk s covers keys [a + 16*T*s, a + 16*T*(s+1)) within
+ * [lo, L_b).  Chunk s writes the SINK-FREE state
+ *   o_part[s, b, h, :] = sum_j exp(s_j - m) v_j / sum_j exp(s_j - m)   (fp32)
+ *   lse_part[s, b, h]  = m + log(sum_j exp(s_j - m))                   (fp32)
+ * with o = 0 and lse = -inf for an empty chunk.  sa_merge_states(... sinks ...)
+ * of these partials equals sa_decode.  Arguments as sa_decode; o_part is
+ * device fp32 [num_splits, batch, num_qo_heads, 64], lse_part device fp32
+ * [num_splits, batch, num_qo_heads].  num_splits >= 1.
+ */
+sa_status_t sa_decode_partial(const void *q, const sa_kv_desc_t *kv, const int32_t *seqlens,
+                              int32_t batch, int32_t num_qo_heads, int32_t max_kv_len,
+                              int32_t window, float sm_scale, int32_t num_splits,
+                              float *o_part, float *lse_part, cudaStream_t stream);
+
+/*
+ * sa_merge_states -- merge S partial attention states with the sink counted once.
+ * Source: "GPT-OSS on day 0", section "Sink Attention": when attention is
+ * split into chunks along the sequence, the sink may enter only once.
+ *   M   = max(sigma_h, max_s lse_part[s, n, h])
+ *   Z   = exp(sigma_h - M) + sum_s exp(lse_part[s, n, h] - M)
+ *   out = sum_s exp(lse_part[s, n, h] - M) o_part[s, n, h, :] / Z   (bf16, RNE)
+ *   lse_out = M + log(Z)
+ * A partial with lse = -inf carries no weight; if every partial is -inf and
+ * there is no sink, out = 0 and lse_out = -inf.
+ *   o_part   device fp32 [num_splits, n, num_heads, head_dim]
+ *   lse_part device fp32 [num_splits, n, num_heads]
+ *   sinks    device fp32 [num_heads] or NULL
+ *   out      device bf16 [n, num_heads, head_dim];  lse_out device fp32 [n, num_heads] or NULL
+ * head_dim must be a multiple of 4 and at most 256; num_splits >= 1.
+ */
+sa_status_t sa_merge_states(const float *o_part, const float *lse_part, int32_t num_splits,
+                            int32_t n, int32_t num_heads, int32_t head_dim,
+                            const float *sinks, void *out, float *lse_out, cudaStream_t stream);
+
+/*
+ * sa_prefill -- causal (or sliding-window) attention of a ragged batch of
+ * query blocks against the KV cache, on tcgen05 tensor cores.
+ * Source: "GPT-OSS on day 0", section "Sink Attention" (prefill and decode
+ * templates both carry the sink); NVIDIA launch article, introduction.
+ *   q            device bf16 [total_q, num_qo_heads, 64], rows of sequence b at
+ *                cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1
+ *   cu_seqlens_q device int32 [batch + 1], cu[0] = 0, non-decreasing
+ *   kv           KV cache descriptor (bf16 only); holds each sequence's keys,
+ *                the queries' own keys included
+ *   seqlens_kv   device int32 [batch]: keys of sequence b (L_kv,b >= L_q,b)
+ *   max_q_len, max_kv_len  host upper bounds on the query / key lengths
+ *   sinks, window, sm_scale  as sa_decode
+ *   out          device bf16 [total_q, num_qo_heads, 64]
+ *   lse          device fp32 [total_q, num_qo_heads] or NULL
+ * Query i of sequence b sits at position L_kv,b - L_q,b + i (bottom-right aligned).
+ * Returns SA_OK, SA_ERR_INVALID_ARG, SA_ERR_UNSUPPORTED or SA_ERR_CUDA.
+ */
+sa_status_t sa_prefill(const void *q, const int32_t *cu_seqlens_q, const sa_kv_desc_t *kv,
+                       const int32_t *seqlens_kv, int32_t batch, int32_t num_qo_heads,
+                       int32_t max_q_len, int32_t max_kv_len, const float *sinks,
+                       int32_t window, float sm_scale, void *out, float *lse,
+                       cudaStream_t stream);
+
+/*
+ * sa_device_status -- synchronise `stream`, then read and clear the device
+ * status word (SA_DEVICE_* bits) of the current device.  The only call that
+ * blocks the host.  Returns SA_OK or SA_ERR_CUDA.
+ */
+sa_status_t sa_device_status(cudaStream_t stream, uint32_t *flags_out);
+
+const char *sa_status_string(sa_status_t status);
+const char *sa_last_error(void);  /* thread-local; "" when none */
+int sa_version(void);             /* SA_VERSION */
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SINK_ATTN_H */

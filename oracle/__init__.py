@@ -76,6 +76,9 @@ def _load():
             lib.sao_attend.restype = ctypes.c_int
             lib.sao_attend.argtypes = [P, ctypes.c_int32, ctypes.c_int32, P, P, ctypes.POINTER(_KV), P,
                                        P, ctypes.c_int32, ctypes.c_double, P, P, ctypes.c_int64, P, P]
+            lib.sao_attend_range.restype = ctypes.c_int
+            lib.sao_attend_range.argtypes = lib.sao_attend.argtypes[:13] + [ctypes.c_int32, ctypes.c_int32,
+                                                                             P, P]
             lib.sao_attend_split.restype = ctypes.c_int
             lib.sao_attend_split.argtypes = [P, ctypes.c_int32, ctypes.c_int32, P, P, ctypes.POINTER(_KV),
                                              P, P, ctypes.c_int32, ctypes.c_double, P, P, ctypes.c_int64,
@@ -175,7 +178,7 @@ def prefill_rows(cu_seqlens_q, seqlens_kv):
 
 # ------------------------------------------------------------------ the math
 def attend(q, row_seq, row_pos, kv: dict, seqlens, sinks, window: int, sm_scale: float,
-           sel_rows=None, sel_heads=None, split=None):
+           sel_rows=None, sel_heads=None, split=None, key_range=None):
     """out [n_sel, D] and lse [n_sel] (fp64) for the selected (row, head) pairs.
 
     q: bf16 [n_rows, Hq, D]; kv: dict with k, v, dtype ('bf16' | 'e4m3'),
@@ -183,6 +186,8 @@ def attend(q, row_seq, row_pos, kv: dict, seqlens, sinks, window: int, sm_scale:
     page_table ([B, max_pages] int32 or None), k_scale, v_scale.
     sel_rows/sel_heads default to every (row, head).  split=(num_chunks, chunk)
     evaluates the chunked form (sink-free partials merged with the sink once).
+    key_range=(lo, hi) restricts the keys to [lo, hi): with sinks=None that is
+    the sink-free partial state of one chunk.
     """
     lib = _load()
     keep = []
@@ -201,7 +206,12 @@ def attend(q, row_seq, row_pos, kv: dict, seqlens, sinks, window: int, sm_scale:
     kvs = _kv_struct(kv, keep)
     out = np.zeros((n_sel, D), np.float64)
     lse = np.zeros((n_sel,), np.float64)
-    if split is None:
+    if key_range is not None:
+        rc = lib.sao_attend_range(_ptr(qa), n_rows, Hq, _ptr(row_seq), _ptr(row_pos), ctypes.byref(kvs),
+                                  _ptr(seqlens), _ptr(sinks_a), int(window), float(sm_scale),
+                                  _ptr(sel_rows), _ptr(sel_heads), n_sel, int(key_range[0]),
+                                  int(key_range[1]), _ptr(out), _ptr(lse))
+    elif split is None:
         rc = lib.sao_attend(_ptr(qa), n_rows, Hq, _ptr(row_seq), _ptr(row_pos), ctypes.byref(kvs),
                             _ptr(seqlens), _ptr(sinks_a), int(window), float(sm_scale),
                             _ptr(sel_rows), _ptr(sel_heads), n_sel, _ptr(out), _ptr(lse))

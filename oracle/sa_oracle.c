@@ -231,18 +231,16 @@ static int attend_one(const uint16_t *qrow, const sao_kv_t *kv, int b, int g, in
  *   sel_row, sel_head [n_sel]; out [n_sel, head_dim] fp64; lse [n_sel] fp64
  * Returns 0, or nonzero on a page table that points outside the pool.
  */
-int sao_attend(const uint16_t *q, int32_t n_rows, int32_t num_qo_heads,
-               const int32_t *row_seq, const int32_t *row_pos,
-               const sao_kv_t *kv, const int32_t *seqlens,
-               const float *sinks, int32_t window, double sm_scale,
-               const int32_t *sel_row, const int32_t *sel_head, int64_t n_sel,
-               double *out, double *lse)
+static int attend_sel(const uint16_t *q, int32_t num_qo_heads, const int32_t *row_seq,
+                      const int32_t *row_pos, const sao_kv_t *kv, const int32_t *seqlens,
+                      const float *sinks, int32_t window, double sm_scale,
+                      const int32_t *sel_row, const int32_t *sel_head, int64_t n_sel,
+                      int32_t j_lo, int32_t j_hi, double *out, double *lse)
 {
     const int D = kv->head_dim;
     const int G = num_qo_heads / kv->num_kv_heads;
     int64_t i;
     int bad = 0;
-    (void)n_rows;
 #pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
     for (i = 0; i < n_sel; ++i) {
         int r = sel_row[i], h = sel_head[i];
@@ -250,9 +248,39 @@ int sao_attend(const uint16_t *q, int32_t n_rows, int32_t num_qo_heads,
         double sigma = sinks ? (double)sinks[h] : -INFINITY;
         const uint16_t *qrow = q + ((int64_t)r * num_qo_heads + h) * D;
         bad |= attend_one(qrow, kv, b, h / G, row_pos[r], seqlens[b], window, sm_scale,
-                          sigma, sinks != NULL, 0, 0x7fffffff, out + i * D, lse + i);
+                          sigma, sinks != NULL, j_lo, j_hi, out + i * D, lse + i);
     }
     return bad;
+}
+
+int sao_attend(const uint16_t *q, int32_t n_rows, int32_t num_qo_heads,
+               const int32_t *row_seq, const int32_t *row_pos,
+               const sao_kv_t *kv, const int32_t *seqlens,
+               const float *sinks, int32_t window, double sm_scale,
+               const int32_t *sel_row, const int32_t *sel_head, int64_t n_sel,
+               double *out, double *lse)
+{
+    (void)n_rows;
+    return attend_sel(q, num_qo_heads, row_seq, row_pos, kv, seqlens, sinks, window, sm_scale,
+                      sel_row, sel_head, n_sel, 0, 0x7fffffff, out, lse);
+}
+
+/*
+ * The same definition restricted to keys j in [j_lo, j_hi) (on top of the
+ * causal/window set), with the sink only when `sinks` is given: the partial
+ * state of one sequence chunk.  With sinks == NULL it is the sink-free state
+ * (o, lse) that a chunk contributes to the merge.
+ */
+int sao_attend_range(const uint16_t *q, int32_t n_rows, int32_t num_qo_heads,
+                     const int32_t *row_seq, const int32_t *row_pos,
+                     const sao_kv_t *kv, const int32_t *seqlens,
+                     const float *sinks, int32_t window, double sm_scale,
+                     const int32_t *sel_row, const int32_t *sel_head, int64_t n_sel,
+                     int32_t j_lo, int32_t j_hi, double *out, double *lse)
+{
+    (void)n_rows;
+    return attend_sel(q, num_qo_heads, row_seq, row_pos, kv, seqlens, sinks, window, sm_scale,
+                      sel_row, sel_head, n_sel, j_lo, j_hi, out, lse);
 }
 
 /*

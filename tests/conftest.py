@@ -27,5 +27,6 @@ def sa():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     import gqa_attention_sinks_head_gb300 as lib
+    lib.build()
     lib.load()
     return lib

@@ -330,6 +330,27 @@ def test_split_invariance(oracle, nsplit):
     assert np.allclose(lse, lse_s, atol=1e-12, rtol=0)
 
 
+def test_key_ranges_merge_to_the_whole(oracle):
+    """Sink-free states of [0, a) and [a, L) merged with the sink = the full row;
+    a range with no visible key is (0, -inf)."""
+    case = W.make_decode_case([1, 90, 500], page_size=16, seed=42, window=0)
+    rows = oracle.decode_rows(case.seqlens)
+    full_o, full_l, _ = run_oracle(oracle, case)
+    kv = case.kv.as_dict()
+    parts = []
+    for lo, hi in [(0, 64), (64, 1 << 30)]:
+        o, l = oracle.attend(case.q, rows[0], rows[1], kv, case.seqlens, None, 0, case.sm_scale,
+                             key_range=(lo, hi))
+        parts.append((o.reshape(3, 64, 64), l.reshape(3, 64)))
+    mo, ml = oracle.merge(np.stack([p[0] for p in parts]), np.stack([p[1] for p in parts]), case.sinks)
+    assert np.allclose(mo, full_o, atol=1e-12) and np.allclose(ml, full_l, atol=1e-12)
+    assert np.all(np.isneginf(parts[1][1][0])) and np.all(parts[1][0][0] == 0)  # L=1: nothing in [64, L)
+    # a range with the sink given is the sink-seeded first chunk of the pages' online form
+    o0, l0 = oracle.attend(case.q, rows[0], rows[1], kv, case.seqlens, case.sinks, 0, case.sm_scale,
+                           key_range=(0, 1 << 30))
+    assert np.array_equal(o0.reshape(3, 64, 64), full_o) and np.array_equal(l0.reshape(3, 64), full_l)
+
+
 def test_split_invariance_window(oracle):
     case = W.make_decode_case([100, 300], page_size=16, seed=41, window=128)
     out, lse, _ = run_oracle(oracle, case)

@@ -292,3 +292,37 @@ def make_config(cfg: int, *, window: int = 0, device="cpu") -> Case:
                                 window=window, seed=seed, device=device,
                                 name="decode B=256 L=8192 paged P=16 fp8-e4m3 w=%d" % window)
     raise ValueError(cfg)
+
+
+def subset(case: Case, seq_ids) -> Case:
+    """CPU copy of the listed sequences only (decode cases): their pages are
+    gathered into a small pool and the table renumbered.  Lets the oracle read
+    a sample of a workload whose cache is too large to copy whole."""
+    kv = case.kv
+    seq_ids = [int(s) for s in seq_ids]
+    L = case.seqlens.cpu()[seq_ids]
+    P = kv.page_size
+    if kv.page_table is None:
+        pages = torch.as_tensor(seq_ids, dtype=torch.long)
+        k = kv.k[pages.to(kv.k.device)].cpu()
+        v = kv.v[pages.to(kv.v.device)].cpu()
+        nkv = KVCache(k, v, kv.dtype, None, P, kv.k_scale, kv.v_scale, kv.layout)
+    else:
+        npg = [(int(l) + P - 1) // P for l in L]
+        table_cpu = kv.page_table.cpu()
+        rows = [table_cpu[s, :n].long() for s, n in zip(seq_ids, npg)]
+        allp = torch.cat(rows) if rows else torch.zeros(0, dtype=torch.long)
+        allp_dev = allp.to(kv.k.device)
+        k = kv.k[allp_dev].cpu()
+        v = kv.v[allp_dev].cpu()
+        if k.shape[0] == 0:  # keep one page so the pool is never empty
+            k, v = kv.k[:1].cpu(), kv.v[:1].cpu()
+        table = torch.zeros(len(seq_ids), max(npg + [1]), dtype=torch.int32)
+        o = 0
+        for i, n in enumerate(npg):
+            table[i, :n] = torch.arange(o, o + n, dtype=torch.int32)
+            o += n
+        nkv = KVCache(k, v, kv.dtype, table, P, kv.k_scale, kv.v_scale, kv.layout)
+    return Case(case.q.cpu()[seq_ids], nkv, L.to(torch.int32),
+                None if case.sinks is None else case.sinks.cpu(), case.window, case.sm_scale,
+                name=case.name + " (sequences %s)" % seq_ids[:8])
