@@ -327,6 +327,105 @@ class DecodeBench:
         return dt, nbytes, desc
 
 
+class PrefillBench:
+    """One step = the prefill calls of the workload (full context, then window 128)."""
+
+    def __init__(self, sa, cfg, device):
+        import torch
+        import workloads as W
+        self.sa, self.cfg, self.torch = sa, cfg, torch
+        self.case = W.make_config(cfg, window=0, device=device)
+        c = self.case
+        self.T, self.Hq, self.D = c.q.shape
+        self.Hkv = c.kv.num_kv_heads
+        cu = c.cu_seqlens_q.cpu()
+        self.q_lens = [int(x) for x in (cu[1:] - cu[:-1])]
+        self.kv_lens = [int(x) for x in c.seqlens.cpu()]
+        self.calls = []
+        for w in windows_of(cfg):
+            out = torch.empty(self.T, self.Hq, self.D, dtype=torch.bfloat16, device=device)
+            lse = torch.empty(self.T, self.Hq, dtype=torch.float32, device=device)
+            self.calls.append(dict(window=w, out=out, lse=lse,
+                                   flops=prefill_flops(self.q_lens, self.kv_lens, w, self.Hq, self.D)))
+        self.step_flops = sum(cl["flops"] for cl in self.calls)
+        self.kernels_per_step = len(self.calls)
+        self.unit = "TFLOP/s"
+        self.elem = 2
+        self.B = len(self.q_lens)
+        self.maxlen = max(self.kv_lens)
+
+    def amount(self):
+        return self.step_flops / 1e12
+
+    def run_call(self, cl, stream, ev=None):
+        c = self.case
+        if ev is not None:
+            ev[0].record(stream)
+        self.sa.sa_prefill(c.q, c.cu_seqlens_q, c.kv, c.seqlens, c.sinks, cl["window"], c.sm_scale, cl["out"],
+                           cl["lse"], max_q_len=max(self.q_lens), max_kv_len=self.maxlen, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+
+    def step(self, stream, evs=None):
+        for i, cl in enumerate(self.calls):
+            self.run_call(cl, stream, None if evs is None else evs[i])
+
+    def dominant(self):
+        return 0, "prefill_kernel", self.calls[0]["flops"]
+
+    def e2e(self, stream, steps, warmup):
+        torch = self.torch
+        c = self.case
+        hq = torch.empty(c.q.shape, dtype=c.q.dtype, pin_memory=True).copy_(c.q.cpu())
+        houts = [(torch.empty(cl["out"].shape, dtype=torch.bfloat16, pin_memory=True),
+                  torch.empty(cl["lse"].shape, dtype=torch.float32, pin_memory=True)) for cl in self.calls]
+        h2d = hq.numel() * 2
+        d2h = sum(o.numel() * 2 + l.numel() * 4 for o, l in houts)
+
+        def one():
+            c.q.copy_(hq, non_blocking=True)
+            for cl, (ho, hl) in zip(self.calls, houts):
+                self.run_call(cl, stream)
+                ho.copy_(cl["out"], non_blocking=True)
+                hl.copy_(cl["lse"], non_blocking=True)
+
+        with torch.cuda.stream(stream):
+            for _ in range(warmup):
+                one()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(steps):
+                one()
+            e1.record(stream)
+            torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps, h2d, d2h
+
+    def oracle_sample(self, budget_s, max_seqs=None):
+        """Rows of the sequence, all heads: the first, then every k-th."""
+        import numpy as np
+        import oracle
+        oracle.build()
+        c = self.case
+        cpu = c.to("cpu")
+        rows = oracle.prefill_rows(cpu.cu_seqlens_q, cpu.seqlens)
+        n = 64 if max_seqs is None else max(1, max_seqs)
+        sel = np.linspace(0, self.T - 1, n).astype(np.int32)
+        t0 = time.time()
+        flops = 0
+        for cl in self.calls:
+            sr = np.repeat(sel, self.Hq)
+            sh = np.tile(np.arange(self.Hq, dtype=np.int32), len(sel))
+            oracle.attend(cpu.q, rows[0], rows[1], cpu.kv.as_dict(), cpu.seqlens, cpu.sinks, cl["window"],
+                          cpu.sm_scale, sr, sh)
+            for r in sel:
+                p = int(rows[1][r])
+                nk = p + 1 if cl["window"] <= 0 else min(cl["window"], p + 1)
+                flops += 4 * self.Hq * self.D * nk
+        dt = time.time() - t0
+        return dt, flops, "%d of %d query rows x %d heads, both calls" % (len(sel), self.T, self.Hq)
+
+
 # ------------------------------------------------------------------- main
 def run_native(args, world, rank, local):
     import torch
@@ -336,9 +435,7 @@ def run_native(args, world, rank, local):
     torch.cuda.set_device(local)
     dist_init(world, "nccl")
     cfg = args.config
-    if cfg == 3:
-        raise SystemExit("prefill bench: sa_prefill is not built yet")
-    wl = DecodeBench(sa, cfg, "cuda")
+    wl = PrefillBench(sa, cfg, "cuda") if cfg == 3 else DecodeBench(sa, cfg, "cuda")
     stream = torch.cuda.Stream()
     steps = args.steps
     sampler = ClockSampler(local) if rank == 0 else None
@@ -370,8 +467,15 @@ def run_native(args, world, rank, local):
 
     peaks, peak_src = load_peaks()
     value = wl.amount() * world / (ms / 1e3)
-    achieved = kbytes / 1e9 / (k_ms / 1e3)
-    peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    if wl.unit == "GB/s":
+        achieved = kbytes / 1e9 / (k_ms / 1e3)
+        peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+        bound, nominal = "hbm", 8000.0
+    else:
+        achieved = kbytes / 1e12 / (k_ms / 1e3)
+        # a kernel looped back to back for the whole timed region: the sustained figure
+        peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+        bound, nominal = "tensor", 2250.0
     traffic = ncu_traffic(kname, "config%d" % cfg)
 
     e2e_ms, h2d, d2h = wl.e2e(stream, max(3, min(steps, 200)), 3)
@@ -384,13 +488,15 @@ def run_native(args, world, rank, local):
         "data": "synthetic (seeded; N(0,1) q/k/v, sinks U(-2,6)); no weights or datasets",
         "config": {"workload": workload_name(cfg), "global_batch": wl.B * world, "seq_len_max": wl.maxlen,
                    "parallelism": "replicas" if world > 1 else "single GPU",
-                   "splits": [cl["S"] for cl in wl.calls],
-                   "l2": "inputs larger than L2 (%.2f GB of KV per step); no flush" % (wl.step_bytes / 1e9)},
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                   "splits": [cl.get("S", 1) for cl in wl.calls],
+                   "l2": ("inputs larger than L2 (%.2f GB of KV per step); no flush" % (wl.step_bytes / 1e9))
+                   if wl.unit == "GB/s" else "compute-bound; no flush"},
+        "roofline": {"bound": bound, "achieved": round(achieved, 1), "peak": peak, "unit": wl.unit,
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": kname, "algorithmic_bytes_per_launch": kbytes,
+                     "kernel": kname, ("algorithmic_bytes_per_launch" if bound == "hbm"
+                                       else "algorithmic_flops_per_launch"): kbytes,
                      "avg_launch_ms": round(k_ms, 6), "peak_source": peak_src,
-                     "frac_of_nominal_8tbs": round(achieved / 8000.0, 4)},
+                     "frac_of_nominal": round(achieved / nominal, 4)},
         "clocks": clocks,
         "e2e": {"value": round(e2e_value, 2), "unit": wl.unit, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "api": "sa_decode with pinned host q/seqlens/page table in, "
@@ -400,7 +506,8 @@ def run_native(args, world, rank, local):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
         dt, nbytes, desc = wl.oracle_sample(30.0)
-        line["cpu_baseline"] = {"value": round(nbytes / 1e9 / dt, 4), "unit": wl.unit,
+        line["cpu_baseline"] = {"value": round(nbytes / (1e9 if wl.unit == "GB/s" else 1e12) / dt, 6),
+                                "unit": wl.unit,
                                 "cores": oracle.num_threads(), "kind": "oracle", "sample": desc,
                                 "seconds": round(dt, 2)}
     if rank == 0:
@@ -419,9 +526,6 @@ def run_reference(args, world, rank, local):
     import gqa_attention_sinks_head_gb300 as sa
     import oracle
     cfg = args.config
-    if cfg == 3:
-        print(json.dumps({"impl": "reference", "unavailable": "prefill oracle arm not wired yet"}))
-        return
     oracle.build()
     sa.build()
     sa.load()
@@ -434,13 +538,13 @@ def run_reference(args, world, rank, local):
         def __getattr__(self, k):
             return getattr(self.inner, k)
 
-    wl = DecodeBench(_Shim(), cfg, dev)
-    total_budget = 120.0
+    wl = PrefillBench(_Shim(), cfg, dev) if cfg == 3 else DecodeBench(_Shim(), cfg, dev)
+    total_budget = float(args.budget_s)
     steps, warmup = args.steps, args.warmup
     # size the per-step sample from a one-sequence pilot
     dt1, b1, _ = wl.oracle_sample(5.0, max_seqs=1)
     per_step = total_budget / max(1, steps + warmup)
-    n = max(1, min(wl.B, int(per_step / max(dt1, 1e-6))))
+    n = max(1, min(wl.B if cfg != 3 else 4096, int(per_step / max(dt1, 1e-6))))
     for _ in range(warmup):
         wl.oracle_sample(per_step, max_seqs=n)
     t0 = time.time()
@@ -450,7 +554,7 @@ def run_reference(args, world, rank, local):
         _, nb, desc = wl.oracle_sample(per_step, max_seqs=n)
         nbytes += nb
     dt = time.time() - t0
-    value = nbytes / 1e9 / dt
+    value = nbytes / (1e9 if wl.unit == "GB/s" else 1e12) / dt
     line = {
         "metric": METRIC, "value": round(value, 4), "unit": wl.unit, "n_gpus": world, "steps": steps,
         "warmup": warmup, "ms_per_step": round(dt / steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
@@ -472,6 +576,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--budget-s", type=float, default=120.0,
+                    help="reference arm: host seconds the whole --steps/--warmup run may take")
     args = ap.parse_args(argv)
     if args.steps is None:
         args.steps = DEFAULT_STEPS[args.config]

@@ -74,7 +74,7 @@ def load(path: str | None = None):
     lib.sa_decode.argtypes = [P, KP, P, i32, i32, i32, P, i32, f32, P, P, P, sz, i32, P]
     lib.sa_decode_partial.argtypes = [P, KP, P, i32, i32, i32, i32, f32, i32, P, P, P]
     lib.sa_merge_states.argtypes = [P, P, i32, i32, i32, i32, P, P, P, P]
-    lib.sa_prefill.argtypes = [P, P, KP, P, i32, i32, i32, i32, P, i32, f32, P, P, P]
+    lib.sa_prefill.argtypes = [P, P, i32, KP, P, i32, i32, i32, i32, P, i32, f32, P, P, P]
     lib.sa_decode_num_splits.argtypes = [i32, i32, i32, i32]
     lib.sa_decode_num_splits.restype = i32
     lib.sa_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32]
@@ -177,7 +177,8 @@ def sa_prefill(q, cu_seqlens_q, kv, seqlens_kv, sinks, window, sm_scale, out, ls
     desc, keep = kv_desc(kv)
     B = int(seqlens_kv.shape[0])
     Hq = int(q.shape[1])
-    _check(lib.sa_prefill(_ptr(q), _ptr(cu_seqlens_q), ctypes.byref(desc), _ptr(seqlens_kv), B, Hq, int(max_q_len),
+    _check(lib.sa_prefill(_ptr(q), _ptr(cu_seqlens_q), int(q.shape[0]), ctypes.byref(desc), _ptr(seqlens_kv), B,
+                          Hq, int(max_q_len),
                           int(max_kv_len), _ptr(sinks), int(window), float(sm_scale), _ptr(out), _ptr(lse),
                           _stream(stream)))
     return out, lse

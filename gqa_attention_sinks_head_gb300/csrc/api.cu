@@ -469,15 +469,88 @@ sa_status_t sa_merge_states(const float *o_part, const float *lse_part, int32_t 
     return SA_OK;
 }
 
-sa_status_t sa_prefill(const void *q, const int32_t *cu_seqlens_q, const sa_kv_desc_t *kv, const int32_t *seqlens_kv,
-                       int32_t batch, int32_t num_qo_heads, int32_t max_q_len, int32_t max_kv_len,
-                       const float *sinks, int32_t window, float sm_scale, void *out, float *lse,
-                       cudaStream_t stream)
+sa_status_t sa_prefill(const void *q, const int32_t *cu_seqlens_q, int32_t total_q, const sa_kv_desc_t *kv,
+                       const int32_t *seqlens_kv, int32_t batch, int32_t num_qo_heads, int32_t max_q_len,
+                       int32_t max_kv_len, const float *sinks, int32_t window, float sm_scale, void *out,
+                       float *lse, cudaStream_t stream)
 {
     g_err[0] = 0;
-    (void)q, (void)cu_seqlens_q, (void)kv, (void)seqlens_kv, (void)batch, (void)num_qo_heads, (void)max_q_len;
-    (void)max_kv_len, (void)sinks, (void)window, (void)sm_scale, (void)out, (void)lse, (void)stream;
-    return fail(SA_ERR_UNSUPPORTED, "sa_prefill is not built yet");
+    if (batch < 0 || total_q < 0 || max_q_len < 0 || max_kv_len < 0 || window < 0)
+        return fail(SA_ERR_INVALID_ARG, "batch, total_q, max_q_len, max_kv_len and window must be >= 0");
+    if (!std::isfinite(sm_scale))
+        return fail(SA_ERR_INVALID_ARG, "sm_scale must be finite");
+    if (batch > 65535)
+        return fail(SA_ERR_UNSUPPORTED, "batch %d > 65535", batch);
+    sa_status_t st = check_kv(kv, batch, num_qo_heads, max_kv_len, false);
+    if (st != SA_OK)
+        return st;
+    if (batch == 0 || total_q == 0 || max_q_len == 0)
+        return SA_OK;
+    if (!q || !cu_seqlens_q || !seqlens_kv || !out)
+        return fail(SA_ERR_INVALID_ARG, "q / cu_seqlens_q / seqlens_kv / out is NULL");
+    if (!aligned16(q) || !aligned16(out))
+        return fail(SA_ERR_UNSUPPORTED, "q and out must be 16-byte aligned");
+    const int group = num_qo_heads / kv->num_kv_heads;
+    sa::PrefillParams p;
+    std::memset(&p, 0, sizeof p);
+    CUtensorMap tq, tk, tv;
+    int dt = 0, dh = 0, dp = 0;
+    st = encode_kv_map(&tk, kv->k, false, kv, 16, &dt, &dh, &dp);
+    if (st != SA_OK)
+        return st;
+    st = encode_kv_map(&tv, kv->v, false, kv, 16, &dt, &dh, &dp);
+    if (st != SA_OK)
+        return st;
+    {
+        EncodeTiledFn fn = encode_fn();
+        if (!fn)
+            return fail(SA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+        const cuuint64_t dims[3] = {static_cast<cuuint64_t>(sa::kHeadDim), static_cast<cuuint64_t>(num_qo_heads),
+                                    static_cast<cuuint64_t>(total_q)};
+        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(sa::kHeadDim) * 2,
+                                       static_cast<cuuint64_t>(num_qo_heads) * sa::kHeadDim * 2};
+        const cuuint32_t box[3] = {static_cast<cuuint32_t>(sa::kHeadDim), 1, 128};
+        const cuuint32_t estr[3] = {1, 1, 1};
+        CUresult r = fn(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(q), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS)
+            return fail(SA_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled rejected q (CUresult %d)", (int)r);
+    }
+    uint32_t *status = nullptr;
+    cudaError_t e = status_ptr(&status);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "device status word");
+    const float kLog2e = 1.44269504088896340736f;
+    p.cu_seqlens_q = cu_seqlens_q;
+    p.seqlens_kv = seqlens_kv;
+    p.page_table = kv->page_table;
+    p.sinks = sinks;
+    p.out = out;
+    p.lse = lse;
+    p.status = status;
+    p.batch = batch;
+    p.num_qo_heads = num_qo_heads;
+    p.num_kv_heads = kv->num_kv_heads;
+    p.group = group;
+    p.heads_per_cta = (group % 2 == 0) ? 2 : 1;  // the two heads of a block share one kv head
+    p.page_size = kv->page_size;
+    p.table_stride = kv->page_table_stride;
+    p.num_pages = kv->num_pages;
+    p.max_q_len = max_q_len;
+    p.max_kv_len = max_kv_len;
+    p.window = window;
+    p.num_q_tiles = (max_q_len + 127) / 128;
+    p.dim_token = dt;
+    p.dim_head = dh;
+    p.dim_page = dp;
+    p.score_scale = sm_scale * kLog2e;
+    if (p.num_q_tiles > 65535)
+        return fail(SA_ERR_UNSUPPORTED, "max_q_len too large");
+    e = sa::launch_prefill(tq, tk, tv, p, stream);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "prefill launch");
+    return SA_OK;
 }
 
 sa_status_t sa_device_status(cudaStream_t stream, uint32_t *flags_out)

@@ -1,0 +1,422 @@
+// prefill.cu -- causal / sliding-window sink-attention prefill on tcgen05.
+//
+// One thread block per (128-query tile, pair of query heads of one kv group,
+// sequence).  The two heads share every K/V tile: the block streams 128-key
+// tiles of K and V through a 3-stage shared-memory ring filled by TMA (16-key
+// boxes, so a paged cache needs no special case), and both heads' products run
+// on the 5th-generation tensor cores with their accumulators in tensor memory:
+//
+//   TMEM columns   0..127  S_0 = Q_0 K^T (fp32), its first 64 columns reused for P_0 (bf16 pairs)
+//                128..255  S_1 / P_1
+//                256..319  O_0 (fp32)      320..383  O_1
+//
+// Warp roles (384 threads):
+//   warp 0      producer: Q tiles once, then K and V tiles (page-table walk, TMA)
+//   warp 1      MMA issuer: S_t = Q_t K^T (SS form), O_t += P_t V (P from TMEM, TS form);
+//               also zeroes the rows of the last V tile that lie past the sequence
+//   warps 4-7   softmax of head 0, warps 8-11 softmax of head 1 (one thread per query row)
+//
+// Per key tile the MMA warp issues, for each head t: PV_t(j) once P_t(j) is in
+// TMEM, then at once QK_t(j+1).  The tensor pipe runs a thread's MMAs in
+// order, so the commit that reports S_t(j+1) also proves that PV_t(j) read
+// P_t(j) and finished writing O_t; the softmax may then rescale O_t.
+//
+// Softmax ("GPT-OSS on day 0" (Perplexity), section "Sink Attention"): each
+// row keeps a running max m (base 2) and sum l, started at the head's sink
+// (m = sink * log2 e, l = 1) so the sink enters the denominator once and has
+// no value vector.  m only moves when a tile's max exceeds it by more than 8
+// (a factor 256): the probabilities then stay below 2^8, the result is the
+// same because numerator and denominator share m, and the O rescale (a TMEM
+// round trip) becomes rare.  Causal and window masks (NVIDIA gpt-oss launch
+// article, introduction: full context alternating with a 128-token window)
+// are applied only on tiles that straddle a boundary.
+#include <cuda_bf16.h>
+
+#include "sa_internal.h"
+#include "sa_ptx.cuh"
+
+namespace sa {
+namespace {
+
+constexpr int BM = 128;  // query rows per tile
+constexpr int BN = 128;  // keys per tile
+constexpr int kStages = 3;
+constexpr int kThreads = 384;
+constexpr uint32_t kTileBytes = BN * kHeadDim * 2;  // 16 KB
+constexpr uint32_t kBoxBytes = 16 * kHeadDim * 2;   // one 16-key box
+constexpr uint32_t kTmemCols = 512;
+__host__ __device__ constexpr uint32_t col_s(int t) { return 128u * t; }         // S_t / P_t
+__host__ __device__ constexpr uint32_t col_o(int t) { return 256u + 64u * t; }   // O_t
+constexpr float kLog2e = 1.44269504088896340736f;
+constexpr float kLn2 = 0.69314718055994530942f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 of the largest tolerated p
+// Registers: 384 threads x 168 at launch = 64512.  The producer/MMA warpgroup
+// drops to 56 and the two softmax warpgroups rise to 224:
+// 128 * 56 + 256 * 224 = 64512.
+constexpr uint32_t kRegsLow = 56;
+constexpr uint32_t kRegsHigh = 224;
+static_assert(128 * kRegsLow + 256 * kRegsHigh <= kThreads * 168, "register split exceeds the launch allocation");
+constexpr uint32_t kIdescQK = idesc_bf16_f32(BM, BN, 0);       // Q, K both K-major
+constexpr uint32_t kIdescPV = idesc_bf16_f32(BM, kHeadDim, 1);  // V is MN-major (dims contiguous)
+
+struct PrefillSmem {
+    uint8_t q[2][kTileBytes];
+    uint8_t k[kStages][kTileBytes];
+    uint8_t v[kStages][kTileBytes];
+    uint64_t q_full;
+    uint64_t k_full[kStages];
+    uint64_t v_full[kStages];
+    uint64_t kv_empty[kStages];
+    uint64_t s_full[2];
+    uint64_t p_full[2];
+    uint64_t o_done[2];
+    uint32_t tmem_base;
+};
+
+__device__ __forceinline__ void kv_coords(const PrefillParams &p, int slot, int g, int page, int &c1, int &c2,
+                                          int &c3)
+{
+    c1 = p.dim_token == 1 ? slot : (p.dim_head == 1 ? g : page);
+    c2 = p.dim_token == 2 ? slot : (p.dim_head == 2 ? g : page);
+    c3 = p.dim_token == 3 ? slot : (p.dim_head == 3 ? g : page);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                   const __grid_constant__ CUtensorMap tmv, const PrefillParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    PrefillSmem &sm =
+        *reinterpret_cast<PrefillSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int NH = p.heads_per_cta;
+    const int h0 = blockIdx.x * NH;
+    const int g = h0 / p.group;
+    const int qt = static_cast<int>(gridDim.y) - 1 - static_cast<int>(blockIdx.y);  // heavy tiles first
+    const int b = blockIdx.z;
+
+    // ---- sequence geometry (uniform over the block) ----------------------
+    const int q_beg = __ldg(p.cu_seqlens_q + b);
+    int Lq = __ldg(p.cu_seqlens_q + b + 1) - q_beg;
+    int Lkv = __ldg(p.seqlens_kv + b);
+    if (Lkv < 0 || Lkv > p.max_kv_len) {
+        if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0)
+            atomicOr(p.status, SA_DEVICE_SEQLEN_RANGE);
+        Lkv = min(max(Lkv, 0), p.max_kv_len);
+    }
+    if (Lq < 0 || Lq > Lkv || Lq > p.max_q_len) {
+        if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0)
+            atomicOr(p.status, SA_DEVICE_BAD_QLEN);
+        Lq = min(max(Lq, 0), min(Lkv, p.max_q_len));
+    }
+    const int q0 = qt * BM;
+    if (q0 >= Lq)
+        return;
+    const int rows = min(BM, Lq - q0);
+    const int off = Lkv - Lq;                 // query i sits at position off + i
+    const int p_first = off + q0;
+    const int p_last = off + q0 + rows - 1;
+    const int k_lo = p.window > 0 ? max(0, p_first - p.window + 1) : 0;
+    const int j_first = k_lo / BN;
+    const int ntiles = p_last / BN - j_first + 1;
+
+    if (threadIdx.x == 0) {
+        mbar_init(&sm.q_full, 1);
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&sm.k_full[i], 1);
+            mbar_init(&sm.v_full[i], 1);
+            mbar_init(&sm.kv_empty[i], 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(&sm.s_full[t], 1);
+            mbar_init(&sm.p_full[t], 4);
+            mbar_init(&sm.o_done[t], 1);
+        }
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&sm.tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sm.tmem_base;
+
+    if (warp < 4) {
+        regs_dec<kRegsLow>();
+    }
+    if (warp == 0) {
+        // ============================ producer ============================
+        if (lane == 0) {
+            tma_prefetch_desc(&tmq);
+            tma_prefetch_desc(&tmk);
+            tma_prefetch_desc(&tmv);
+            mbar_arrive_expect_tx(&sm.q_full, static_cast<uint32_t>(NH) * kTileBytes);
+            for (int t = 0; t < NH; ++t)
+                tma_load_3d(sm.q[t], &tmq, &sm.q_full, 0, h0 + t, q_beg + q0);
+        }
+        const int32_t *trow = p.page_table ? p.page_table + static_cast<int64_t>(b) * p.table_stride : nullptr;
+        auto boxes = [&](int it) { return min(BN / 16, (Lkv - (j_first + it) * BN + 15) / 16); };
+        auto page_of = [&](int it) -> int {
+            if (it >= ntiles || lane >= boxes(it))
+                return 0;
+            const int key = (j_first + it) * BN + 16 * lane;
+            return trow ? __ldg(trow + key / p.page_size) : b;
+        };
+        int next_page = page_of(0);
+        for (int it = 0; it < ntiles; ++it) {
+            const int stage = it % kStages;
+            const int page = next_page;
+            const int nbox = boxes(it);
+            next_page = page_of(it + 1);  // one tile ahead: the table read overlaps the wait
+            if (it >= kStages && !mbar_wait(&sm.kv_empty[stage], ((it / kStages) - 1) & 1, p.status))
+                break;
+            const int key = (j_first + it) * BN + 16 * lane;
+            int c1 = 0, c2 = 0, c3 = 0;
+            if (lane < nbox) {
+                if (page < 0 || page >= p.num_pages)
+                    atomicOr(p.status, SA_DEVICE_BAD_PAGE);  // outside the map: the box reads zeros
+                kv_coords(p, key % p.page_size, g, page, c1, c2, c3);
+            }
+            if (lane == 0)
+                mbar_arrive_expect_tx(&sm.k_full[stage], static_cast<uint32_t>(nbox) * kBoxBytes);
+            __syncwarp();
+            if (lane < nbox)
+                tma_load_4d(sm.k[stage] + lane * kBoxBytes, &tmk, &sm.k_full[stage], 0, c1, c2, c3);
+            if (lane == 0)
+                mbar_arrive_expect_tx(&sm.v_full[stage], static_cast<uint32_t>(nbox) * kBoxBytes);
+            __syncwarp();
+            if (lane < nbox)
+                tma_load_4d(sm.v[stage] + lane * kBoxBytes, &tmv, &sm.v_full[stage], 0, c1, c2, c3);
+        }
+    } else if (warp == 1) {
+        // ============================ MMA issuer ==========================
+        const uint32_t qaddr[2] = {smem_u32(sm.q[0]), smem_u32(sm.q[1])};
+        auto issue_qk = [&](int t, int stage) {
+            const uint32_t ka = smem_u32(sm.k[stage]);
+#pragma unroll
+            for (int ks = 0; ks < kHeadDim / 16; ++ks)  // K = 16 dims (32 bytes) per instruction
+                umma_ss(tmem + col_s(t), smem_desc_sw128(qaddr[t] + 32 * ks, 16, 1024),
+                        smem_desc_sw128(ka + 32 * ks, 16, 1024), kIdescQK, ks > 0 ? 1u : 0u);
+        };
+        auto issue_pv = [&](int t, int stage, bool accumulate) {
+            const uint32_t va = smem_u32(sm.v[stage]);
+#pragma unroll
+            for (int kk = 0; kk < BN / 16; ++kk)  // K = 16 keys: 8 TMEM columns of P, 2 KB of V
+                umma_ts(tmem + col_o(t), tmem + col_s(t) + 8 * kk, smem_desc_sw128(va + 2048 * kk, 16, 1024),
+                        kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
+        };
+        bool ok = mbar_wait(&sm.q_full, 0, p.status) && mbar_wait(&sm.k_full[0], 0, p.status);
+        if (ok) {
+            tc_fence_after();
+            if (lane == 0)
+                for (int t = 0; t < NH; ++t) {
+                    issue_qk(t, 0);
+                    umma_commit(&sm.s_full[t]);
+                }
+            __syncwarp();
+        }
+        for (int it = 0; ok && it < ntiles; ++it) {
+            const int stage = it % kStages;
+            if (!mbar_wait(&sm.v_full[stage], (it / kStages) & 1, p.status)) {
+                ok = false;
+                break;
+            }
+            const int key0 = (j_first + it) * BN;
+            if (key0 + BN > Lkv) {
+                // value rows past the sequence may hold anything (NaN included):
+                // zero them so that p = 0 contributes exactly 0
+                const int first_bad = max(Lkv - key0, 0);
+                uint4 *vz = reinterpret_cast<uint4 *>(sm.v[stage]);
+                for (int i = first_bad * 8 + lane; i < BN * 8; i += 32)
+                    vz[i] = make_uint4(0u, 0u, 0u, 0u);
+                fence_proxy_async_smem();
+                __syncwarp();
+            }
+            for (int t = 0; t < NH; ++t) {
+                if (!mbar_wait(&sm.p_full[t], it & 1, p.status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (lane == 0)
+                    issue_pv(t, stage, it > 0);
+                if (it + 1 < ntiles) {
+                    const int ns = (it + 1) % kStages;
+                    if (!mbar_wait(&sm.k_full[ns], ((it + 1) / kStages) & 1, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    if (lane == 0) {
+                        issue_qk(t, ns);
+                        umma_commit(&sm.s_full[t]);
+                    }
+                }
+                __syncwarp();
+            }
+            if (lane == 0)
+                umma_commit(&sm.kv_empty[stage]);
+            __syncwarp();
+        }
+        if (lane == 0)
+            for (int t = 0; t < NH; ++t)
+                umma_commit(&sm.o_done[t]);
+        __syncwarp();
+    } else if (warp >= 4) {
+        // ============================ softmax =============================
+        regs_inc<kRegsHigh>();
+        const int t = (warp - 4) >> 2;
+        if (t < NH) {
+        const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
+        const int row = quarter * 32 + lane;
+        const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+        const uint32_t s_addr = tmem + lane_base + col_s(t);
+        const uint32_t o_addr = tmem + lane_base + col_o(t);
+        const int qi = q0 + row;
+        const int pos = off + qi;
+        const int h = h0 + t;
+        float m = -INFINITY, l = 0.f;
+        if (p.sinks) {
+            m = __ldg(p.sinks + h) * kLog2e;  // the running max starts at the sink ...
+            l = 1.f;                          // ... and the sum at 1
+        }
+        bool ok = true;
+        for (int it = 0; it < ntiles; ++it) {
+            if (!mbar_wait(&sm.s_full[t], it & 1, p.status)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t sr[4][32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                tmem_ld32(s_addr + 32 * c, sr[c]);
+            tmem_ld_wait();
+            const int key0 = (j_first + it) * BN;
+            const bool edge =
+                key0 + BN - 1 > p_first || (p.window > 0 && key0 <= p_last - p.window) || key0 + BN > Lkv;
+            float mt = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    float s = __uint_as_float(sr[c][i]) * p.score_scale;
+                    if (edge) {
+                        const int key = key0 + 32 * c + i;
+                        const bool vis = key <= pos && key < Lkv && (p.window <= 0 || key > pos - p.window);
+                        s = vis ? s : -INFINITY;
+                    }
+                    sr[c][i] = __float_as_uint(s);
+                    mt = fmaxf(mt, s);
+                }
+            const bool upd = mt > m + kRescaleThreshold;
+            if (__any_sync(0xffffffffu, upd)) {
+                const float mn = upd ? mt : m;
+                const float alpha = upd ? ex2(m - mn) : 1.f;
+                l *= alpha;
+                if (it > 0) {  // O holds earlier tiles: bring it to the new max
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        uint32_t ov[32];
+                        tmem_ld32(o_addr + 32 * c, ov);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+                        tmem_st32(o_addr + 32 * c, ov);
+                    }
+                }
+                m = mn;
+            }
+            const float mu = m == -INFINITY ? 0.f : m;
+            uint32_t pk[2][32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) {
+                    const float p0 = ex2(__uint_as_float(sr[c][i]) - mu);
+                    const float p1 = ex2(__uint_as_float(sr[c][i + 1]) - mu);
+                    l += p0 + p1;
+                    pk[c >> 1][(c & 1) * 16 + (i >> 1)] = pack_bf16(p0, p1);
+                }
+            tmem_st32(s_addr, pk[0]);  // P overwrites the first 64 columns of S
+            tmem_st32(s_addr + 32, pk[1]);
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&sm.p_full[t]);
+        }
+        // ---- epilogue: O / l, lse = (m + log2 l) ln 2 ----
+        if (ok && mbar_wait(&sm.o_done[t], 0, p.status)) {
+            tc_fence_after();
+            uint32_t ov[2][32];
+            tmem_ld32(o_addr, ov[0]);
+            tmem_ld32(o_addr + 32, ov[1]);
+            tmem_ld_wait();
+            if (qi < Lq) {
+                const float inv = l > 0.f ? 1.f / l : 0.f;
+                const int64_t orow = static_cast<int64_t>(q_beg + qi) * p.num_qo_heads + h;
+                uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.out) + orow * kHeadDim);
+#pragma unroll
+                for (int c = 0; c < 2; ++c)
+#pragma unroll
+                    for (int v4 = 0; v4 < 4; ++v4) {
+                        uint4 w;
+                        w.x = pack_bf16(__uint_as_float(ov[c][8 * v4 + 0]) * inv, __uint_as_float(ov[c][8 * v4 + 1]) * inv);
+                        w.y = pack_bf16(__uint_as_float(ov[c][8 * v4 + 2]) * inv, __uint_as_float(ov[c][8 * v4 + 3]) * inv);
+                        w.z = pack_bf16(__uint_as_float(ov[c][8 * v4 + 4]) * inv, __uint_as_float(ov[c][8 * v4 + 5]) * inv);
+                        w.w = pack_bf16(__uint_as_float(ov[c][8 * v4 + 6]) * inv, __uint_as_float(ov[c][8 * v4 + 7]) * inv);
+                        dst[c * 4 + v4] = w;
+                    }
+                if (p.lse)
+                    p.lse[orow] = l > 0.f ? (m + lg2(l)) * kLn2 : -INFINITY;
+            }
+        }
+        }
+    }
+
+    // ---- teardown: every TMEM access is done before the columns are freed ----
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+size_t prefill_smem_bytes() { return sizeof(PrefillSmem) + 1024; }
+
+cudaError_t prepare_prefill()
+{
+    static int done[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev >= 0 && dev < 64 && done[dev])
+        return cudaSuccess;
+    e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(prefill_smem_bytes()));
+    if (e == cudaSuccess && dev >= 0 && dev < 64)
+        done[dev] = 1;
+    return e;
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                           const PrefillParams &p, cudaStream_t stream)
+{
+    cudaError_t e = prepare_prefill();
+    if (e != cudaSuccess)
+        return e;
+    const dim3 grid(p.num_qo_heads / p.heads_per_cta, p.num_q_tiles, p.batch);
+    prefill_kernel<<<grid, kThreads, prefill_smem_bytes(), stream>>>(tq, tk, tv, p);
+    return cudaGetLastError();
+}
+
+}  // namespace sa

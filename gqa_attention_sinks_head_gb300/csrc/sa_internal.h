@@ -46,14 +46,15 @@ struct PrefillParams {
     const int32_t *cu_seqlens_q;  // [B+1]
     const int32_t *seqlens_kv;    // [B]
     const int32_t *page_table;    // [B, table_stride] or nullptr
-    const float *sinks;
-    void *out;                    // bf16 [Tq, Hq, 64]
-    float *lse;                   // [Tq, Hq] or nullptr
+    const float *sinks;           // [Hq] or nullptr
+    void *out;                    // bf16 [total_q, Hq, 64]
+    float *lse;                   // [total_q, Hq] or nullptr
     uint32_t *status;
-    int32_t batch, num_qo_heads, num_kv_heads, group;
+    int32_t batch, num_qo_heads, num_kv_heads, group, heads_per_cta;
     int32_t page_size, table_stride, num_pages, max_q_len, max_kv_len;
     int32_t window, num_q_tiles;
-    float score_scale;            // sm_scale * log2(e)
+    int32_t dim_token, dim_head, dim_page;  // tensor-map dimension (1..3) of each KV coordinate
+    float score_scale;                      // sm_scale * log2(e)
 };
 
 // Launchers (return the launch error, if any).

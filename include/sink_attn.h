@@ -212,6 +212,8 @@ sa_status_t sa_merge_states(const float *o_part, const float *lse_part, int32_t 
  *   q            device bf16 [total_q, num_qo_heads, 64], rows of sequence b at
  *                cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1
  *   cu_seqlens_q device int32 [batch + 1], cu[0] = 0, non-decreasing
+ *   total_q      rows of q and out (= cu_seqlens_q[batch]); the kernels read and
+ *                write no row at or past it
  *   kv           KV cache descriptor (bf16 only); holds each sequence's keys,
  *                the queries' own keys included
  *   seqlens_kv   device int32 [batch]: keys of sequence b (L_kv,b >= L_q,b)
@@ -222,7 +224,7 @@ sa_status_t sa_merge_states(const float *o_part, const float *lse_part, int32_t 
  * Query i of sequence b sits at position L_kv,b - L_q,b + i (bottom-right aligned).
  * Returns SA_OK, SA_ERR_INVALID_ARG, SA_ERR_UNSUPPORTED or SA_ERR_CUDA.
  */
-sa_status_t sa_prefill(const void *q, const int32_t *cu_seqlens_q, const sa_kv_desc_t *kv,
+sa_status_t sa_prefill(const void *q, const int32_t *cu_seqlens_q, int32_t total_q, const sa_kv_desc_t *kv,
                        const int32_t *seqlens_kv, int32_t batch, int32_t num_qo_heads,
                        int32_t max_q_len, int32_t max_kv_len, const float *sinks,
                        int32_t window, float sm_scale, void *out, float *lse,

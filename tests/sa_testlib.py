@@ -71,3 +71,29 @@ def oracle_decode(oracle, case_cpu, sel_rows=None):
 
 def compact_decode_case(case, seq_ids) -> W.Case:
     return W.subset(case, seq_ids)
+
+
+def prefill_gpu(sa, case_gpu, with_lse=True):
+    T, Hq, D = case_gpu.q.shape
+    out = torch.full((T, Hq, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((T, Hq), float("nan"), dtype=torch.float32, device="cuda") if with_lse else None
+    cu = case_gpu.cu_seqlens_q
+    qlens = (cu[1:] - cu[:-1]).cpu()
+    sa.sa_prefill(case_gpu.q, cu, case_gpu.kv, case_gpu.seqlens, case_gpu.sinks, case_gpu.window,
+                  case_gpu.sm_scale, out, lse, max_q_len=int(qlens.max()) if len(qlens) else 0,
+                  max_kv_len=int(case_gpu.seqlens.max()) if len(qlens) else 0)
+    torch.cuda.synchronize()
+    return out, lse
+
+
+def oracle_prefill(oracle, case_cpu, sel_rows=None):
+    rows = oracle.prefill_rows(case_cpu.cu_seqlens_q, case_cpu.seqlens)
+    T, Hq, D = case_cpu.q.shape
+    if sel_rows is None:
+        sel_rows = np.arange(T, dtype=np.int32)
+    sel_rows = np.asarray(sel_rows, np.int32)
+    sr = np.repeat(sel_rows, Hq)
+    sh = np.tile(np.arange(Hq, dtype=np.int32), len(sel_rows))
+    out, lse = oracle.attend(case_cpu.q, rows[0], rows[1], case_cpu.kv.as_dict(), case_cpu.seqlens,
+                             case_cpu.sinks, case_cpu.window, case_cpu.sm_scale, sr, sh)
+    return out.reshape(len(sel_rows), Hq, D), lse.reshape(len(sel_rows), Hq)
