@@ -15,7 +15,7 @@ import os
 
 __all__ = [
     "SinkAttnError", "KVDesc", "load", "build", "sa_decode", "sa_decode_partial", "sa_merge_states",
-    "sa_prefill", "sa_decode_num_splits", "sa_decode_workspace_size", "sa_device_status", "sa_version",
+    "sa_prefill", "sa_decode_static_workspace", "sa_decode_num_splits", "sa_decode_workspace_size", "sa_device_status", "sa_version",
     "SA_KV_BF16", "SA_KV_FP8_E4M3", "kv_desc",
 ]
 
@@ -28,7 +28,8 @@ SA_DEVICE_SEQLEN_RANGE, SA_DEVICE_BAD_PAGE, SA_DEVICE_TIMEOUT, SA_DEVICE_BAD_QLE
 
 EXPORTS = ["sa_decode", "sa_decode_num_splits", "sa_decode_workspace_size", "sa_decode_partial",
            "sa_merge_states", "sa_prefill", "sa_device_status", "sa_status_string", "sa_last_error",
-           "sa_version"]
+           "sa_version", "sa_decode_static_workspace"]
+SA_STATIC_WORKSPACE_BYTES = 16 << 20
 
 
 class SinkAttnError(RuntimeError):
@@ -72,6 +73,7 @@ def load(path: str | None = None):
     P, i32, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
     KP = ctypes.POINTER(KVDesc)
     lib.sa_decode.argtypes = [P, KP, P, i32, i32, i32, P, i32, f32, P, P, P, sz, i32, P]
+    lib.sa_decode_static_workspace.argtypes = [P, KP, P, i32, i32, i32, P, i32, f32, P, P, i32, P]
     lib.sa_decode_partial.argtypes = [P, KP, P, i32, i32, i32, i32, f32, i32, P, P, P]
     lib.sa_merge_states.argtypes = [P, P, i32, i32, i32, i32, P, P, P, P]
     lib.sa_prefill.argtypes = [P, P, i32, KP, P, i32, i32, i32, i32, P, i32, f32, P, P, P]
@@ -84,7 +86,7 @@ def load(path: str | None = None):
     lib.sa_status_string.restype = ctypes.c_char_p
     lib.sa_last_error.restype = ctypes.c_char_p
     lib.sa_version.restype = ctypes.c_int
-    for fn in ("sa_decode", "sa_decode_partial", "sa_merge_states", "sa_prefill", "sa_device_status"):
+    for fn in ("sa_decode", "sa_decode_static_workspace", "sa_decode_partial", "sa_merge_states", "sa_prefill", "sa_device_status"):
         getattr(lib, fn).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -151,6 +153,19 @@ def sa_decode(q, kv, seqlens, sinks, window, sm_scale, out, lse=None, *, max_kv_
     _check(lib.sa_decode(_ptr(q), ctypes.byref(desc), _ptr(seqlens), B, Hq, int(max_kv_len), _ptr(sinks),
                          int(window), float(sm_scale), _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes,
                          int(num_splits), _stream(stream)))
+    return out, lse
+
+
+def sa_decode_static_workspace(q, kv, seqlens, sinks, window, sm_scale, out, lse=None, *, max_kv_len,
+                               num_splits=0, stream=None):
+    """sa_decode with the split scratch in the library's own static device
+    array (for callers that cannot allocate); see include/sink_attn.h."""
+    lib = load()
+    desc, keep = kv_desc(kv)
+    B, Hq, _ = q.shape
+    _check(lib.sa_decode_static_workspace(_ptr(q), ctypes.byref(desc), _ptr(seqlens), B, Hq, int(max_kv_len),
+                                          _ptr(sinks), int(window), float(sm_scale), _ptr(out), _ptr(lse),
+                                          int(num_splits), _stream(stream)))
     return out, lse
 
 

@@ -334,6 +334,15 @@ sa_status_t launch_decode_kernel(const void *q, const sa_kv_desc_t *kv, const in
 
 }  // namespace
 
+sa_status_t sa::set_last_error(sa_status_t st, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return st;
+}
+
 extern "C" {
 
 const char *sa_status_string(sa_status_t s)

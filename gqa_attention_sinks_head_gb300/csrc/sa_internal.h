@@ -6,6 +6,8 @@
 #include <cuda_runtime_api.h>
 #include <stdint.h>
 
+#include "../../include/sink_attn.h"
+
 namespace sa {
 
 constexpr int kHeadDim = 64;   // the kernels handle head_dim 64 only
@@ -56,6 +58,9 @@ struct PrefillParams {
     int32_t dim_token, dim_head, dim_page;  // tensor-map dimension (1..3) of each KV coordinate
     float score_scale;                      // sm_scale * log2(e)
 };
+
+// Record `fmt` as the calling thread's sa_last_error() message and return st.
+sa_status_t set_last_error(sa_status_t st, const char *fmt, ...);
 
 // Launchers (return the launch error, if any).
 cudaError_t launch_decode(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p,

@@ -231,6 +231,38 @@ sa_status_t sa_prefill(const void *q, const int32_t *cu_seqlens_q, int32_t total
                        cudaStream_t stream);
 
 /*
+ * sa_decode_static_workspace -- sa_decode for callers that cannot allocate
+ * device memory.  The pages have no counterpart; this is an interface
+ * convenience of the library.
+ *
+ * A split decode needs scratch for its per-chunk partial states, which
+ * sa_decode takes from the caller.  Some callers cannot provide it: a plugin
+ * inside a host program that owns all device memory and hands it only its
+ * input and output tensors, or a caller on a latency-critical path that must
+ * not call cudaMalloc (it may synchronise the device).  This entry point keeps
+ * the scratch in a fixed array of SA_STATIC_WORKSPACE_BYTES in device memory
+ * that the library declares itself; every GPU that loads the library holds that
+ * array until the process exits.  It calls no allocator.
+ *
+ * Arguments, results and errors are those of sa_decode without the workspace
+ * pair.  A split that needs more than SA_STATIC_WORKSPACE_BYTES of scratch
+ * (see sa_decode_workspace_size) is refused with SA_ERR_WORKSPACE before any
+ * launch; ask for fewer chunks or use sa_decode.  The first call on each
+ * device looks up the array's device address (cudaGetSymbolAddress); make that
+ * first call before any stream capture on that device.
+ *
+ * All calls share the one array and it keeps whatever the last call left in
+ * it.  Nothing in it needs to start at zero (each call writes every entry it
+ * later reads), but two calls whose work overlaps on the GPU -- on different
+ * streams, or from different threads -- race on it: order them.
+ */
+#define SA_STATIC_WORKSPACE_BYTES (16u << 20) /* 16 MiB */
+sa_status_t sa_decode_static_workspace(const void *q, const sa_kv_desc_t *kv, const int32_t *seqlens,
+                                       int32_t batch, int32_t num_qo_heads, int32_t max_kv_len,
+                                       const float *sinks, int32_t window, float sm_scale, void *out,
+                                       float *lse, int32_t num_splits, cudaStream_t stream);
+
+/*
  * sa_device_status -- synchronise `stream`, then read and clear the device
  * status word (SA_DEVICE_* bits) of the current device.  The only call that
  * blocks the host.  Returns SA_OK or SA_ERR_CUDA.
