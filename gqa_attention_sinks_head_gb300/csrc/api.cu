@@ -488,6 +488,8 @@ sa_status_t sa_prefill(const void *q, const int32_t *cu_seqlens_q, int32_t total
         return fail(SA_ERR_INVALID_ARG, "batch, total_q, max_q_len, max_kv_len and window must be >= 0");
     if (!std::isfinite(sm_scale))
         return fail(SA_ERR_INVALID_ARG, "sm_scale must be finite");
+    if (!(sm_scale > 0.f))
+        return fail(SA_ERR_UNSUPPORTED, "sa_prefill needs sm_scale > 0");
     if (batch > 65535)
         return fail(SA_ERR_UNSUPPORTED, "batch %d > 65535", batch);
     sa_status_t st = check_kv(kv, batch, num_qo_heads, max_kv_len, false);

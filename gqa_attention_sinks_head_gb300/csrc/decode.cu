@@ -35,6 +35,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <cstdlib>
+
 #include "sa_internal.h"
 #include "sa_ptx.cuh"
 
@@ -42,8 +44,12 @@ namespace sa {
 namespace {
 
 constexpr int kConsumerWarps = 4;
-constexpr int kStages = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
+// Pipeline depth.  3 stages x 4 resident blocks per SM keep as many bytes in
+// flight as 4 x 3 (192 KB of bf16 K/V per SM), with more blocks to hide the
+// per-block prologue and fewer waves for short (window) calls.  FP8 tiles are
+// half the size, so the FP8 kernel runs twice the stages for the same bytes.
+constexpr int kDefaultStages = 3;
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kLog2e = 1.44269504088896340736f;
 
@@ -53,7 +59,7 @@ struct DecodeCfg {
     static constexpr int kTileBytes = kTile * kRowBytes;        // 1 KB or 2 KB
 };
 
-template <bool FP8>
+template <bool FP8, int kStages>
 struct DecodeSmem {
     // K and V tiles of each stage, one per consumer warp (1 KB aligned).
     uint8_t k[kStages][kConsumerWarps][DecodeCfg<FP8>::kTileBytes];
@@ -65,8 +71,8 @@ struct DecodeSmem {
 };
 // The per-warp O^T partials of the final merge reuse the K tiles.
 static_assert(sizeof(float) * kConsumerWarps * kHeadDim * kMaxGroup <=
-                  sizeof(uint8_t) * kStages * kConsumerWarps * DecodeCfg<true>::kTileBytes,
-              "merge scratch must fit in the K tiles");
+                  sizeof(uint8_t) * 2 * kConsumerWarps * DecodeCfg<true>::kTileBytes,
+              "merge scratch must fit in the K tiles of two stages");
 
 // Byte offset of 16-byte chunk `chunk` of row `row` in a swizzled tile.
 template <bool FP8>
@@ -78,15 +84,16 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk)
         return row * 128 + ((chunk ^ (row & 7)) << 4);
 }
 
-template <bool FP8>
-__global__ void __launch_bounds__(kThreads, 3) decode_kernel(const __grid_constant__ CUtensorMap tmk,
+template <bool FP8, int kStages>
+__global__ void __launch_bounds__(kThreads, 4) decode_kernel(const __grid_constant__ CUtensorMap tmk,
                                                              const __grid_constant__ CUtensorMap tmv,
                                                              const DecodeParams p)
 {
     using Cfg = DecodeCfg<FP8>;
     extern __shared__ uint8_t smem_raw[];
-    DecodeSmem<FP8> &sm =
-        *reinterpret_cast<DecodeSmem<FP8> *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    static_assert(kStages >= 2, "merge scratch needs two stages of K tiles");
+    DecodeSmem<FP8, kStages> &sm =
+        *reinterpret_cast<DecodeSmem<FP8, kStages> *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -401,15 +408,18 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const __grid_consta
             }
         }
     }
+    // This block's outputs are written: a programmatically dependent grid
+    // (the merge of a split decode) may start launching.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-template <bool FP8>
+template <bool FP8, int kStages>
 size_t decode_smem_bytes()
 {
-    return sizeof(DecodeSmem<FP8>) + 1024;  // + slack for the 1 KB alignment
+    return sizeof(DecodeSmem<FP8, kStages>) + 1024;  // + slack for the 1 KB alignment
 }
 
-template <bool FP8>
+template <bool FP8, int kStages>
 cudaError_t prepare_decode()
 {
     // one cudaFuncSetAttribute per device and variant
@@ -420,44 +430,59 @@ cudaError_t prepare_decode()
         return e;
     if (dev >= 0 && dev < 64 && done[dev])
         return cudaSuccess;
-    e = cudaFuncSetAttribute(decode_kernel<FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(decode_smem_bytes<FP8>()));
+    e = cudaFuncSetAttribute(decode_kernel<FP8, kStages>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(decode_smem_bytes<FP8, kStages>()));
     if (e == cudaSuccess && dev >= 0 && dev < 64)
         done[dev] = 1;
     return e;
+}
+
+// SA_DECODE_STAGES (3 or 4): pipeline depth, a tuning knob; default 3.
+int decode_stages()
+{
+    static const int st = [] {
+        const char *v = std::getenv("SA_DECODE_STAGES");
+        return (v && std::atoi(v) == 4) ? 4 : kDefaultStages;
+    }();
+    return st;
+}
+
+template <bool FP8, int kStages>
+cudaError_t occupancy_of(int *blocks_per_sm)
+{
+    cudaError_t e = prepare_decode<FP8, kStages>();
+    if (e != cudaSuccess)
+        return e;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, decode_kernel<FP8, kStages>, kThreads,
+                                                         decode_smem_bytes<FP8, kStages>());
+}
+
+template <bool FP8, int kStages>
+cudaError_t launch_of(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p, cudaStream_t stream)
+{
+    cudaError_t e = prepare_decode<FP8, kStages>();
+    if (e != cudaSuccess)
+        return e;
+    const dim3 grid(p.num_splits, p.num_kv_heads, p.batch);
+    decode_kernel<FP8, kStages><<<grid, kThreads, decode_smem_bytes<FP8, kStages>(), stream>>>(tk, tv, p);
+    return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t decode_occupancy(bool fp8, int *blocks_per_sm)
 {
-    cudaError_t e = fp8 ? prepare_decode<true>() : prepare_decode<false>();
-    if (e != cudaSuccess)
-        return e;
-    if (fp8)
-        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, decode_kernel<true>, kThreads,
-                                                             decode_smem_bytes<true>());
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, decode_kernel<false>, kThreads,
-                                                         decode_smem_bytes<false>());
+    if (decode_stages() == 4)
+        return fp8 ? occupancy_of<true, 8>(blocks_per_sm) : occupancy_of<false, 4>(blocks_per_sm);
+    return fp8 ? occupancy_of<true, 6>(blocks_per_sm) : occupancy_of<false, 3>(blocks_per_sm);
 }
 
 cudaError_t launch_decode(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p, bool fp8,
                           cudaStream_t stream)
 {
-    const dim3 grid(p.num_splits, p.num_kv_heads, p.batch);
-    cudaError_t e;
-    if (fp8) {
-        e = prepare_decode<true>();
-        if (e != cudaSuccess)
-            return e;
-        decode_kernel<true><<<grid, kThreads, decode_smem_bytes<true>(), stream>>>(tk, tv, p);
-    } else {
-        e = prepare_decode<false>();
-        if (e != cudaSuccess)
-            return e;
-        decode_kernel<false><<<grid, kThreads, decode_smem_bytes<false>(), stream>>>(tk, tv, p);
-    }
-    return cudaGetLastError();
+    if (decode_stages() == 4)
+        return fp8 ? launch_of<true, 8>(tk, tv, p, stream) : launch_of<false, 4>(tk, tv, p, stream);
+    return fp8 ? launch_of<true, 6>(tk, tv, p, stream) : launch_of<false, 3>(tk, tv, p, stream);
 }
 
 }  // namespace sa

@@ -21,6 +21,10 @@ constexpr int kMergeWarps = 8;
 
 __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergeParams p)
 {
+    // Launched as a programmatic dependent of the split decode: wait here until
+    // that grid has finished and its partial states are visible (returns at
+    // once when there is no such dependency).
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int lane = threadIdx.x & 31;
     const int64_t NH = static_cast<int64_t>(p.n) * p.num_heads;
     const int64_t row = static_cast<int64_t>(blockIdx.x) * kMergeWarps + (threadIdx.x >> 5);
@@ -28,34 +32,49 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergePara
         return;
     const int h = static_cast<int>(row % p.num_heads);
     const float sigma = p.sinks ? __ldg(p.sinks + h) : -INFINITY;
+    const int S = p.num_splits;
+    const int D = p.head_dim;
 
-    float M = sigma;
-    for (int s = lane; s < p.num_splits; s += 32)
+    // lane s holds lse of chunk s (chunks past 32 fold in below)
+    float ls = lane < S ? __ldg(p.lse_part + lane * NH + row) : -INFINITY;
+    float M = fmaxf(sigma, ls);
+    for (int s = lane + 32; s < S; s += 32)
         M = fmaxf(M, __ldg(p.lse_part + s * NH + row));
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1)
         M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
 
-    const int D = p.head_dim;
     __nv_bfloat16 *out = reinterpret_cast<__nv_bfloat16 *>(p.out) + row * D;
     if (M == -INFINITY) {  // no key anywhere and no sink
-        for (int d = 4 * lane; d < D; d += 128) {
-            out[d] = out[d + 1] = out[d + 2] = out[d + 3] = __float2bfloat16(0.f);
-        }
+        for (int d = 4 * lane; d < D; d += 128)
+            *reinterpret_cast<uint2 *>(out + d) = make_uint2(0u, 0u);
         if (lane == 0 && p.lse_out)
             p.lse_out[row] = -INFINITY;
         return;
     }
-    float Z = sigma == -INFINITY ? 0.f : expf(sigma - M);
-    // up to 256 dims: two float4 per lane
+    // weights: lane s holds exp(lse_s - M) for the first 32 chunks
+    const float w_lane = ls == -INFINITY ? 0.f : expf(ls - M);
+    float Z = w_lane;
+    for (int s = lane + 32; s < S; s += 32) {
+        const float l2 = __ldg(p.lse_part + s * NH + row);
+        Z += l2 == -INFINITY ? 0.f : expf(l2 - M);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+        Z += __shfl_xor_sync(0xffffffffu, Z, off);
+    Z += sigma == -INFINITY ? 0.f : expf(sigma - M);
+
+    // every lane accumulates a float4 slice (two slices when D > 128); the
+    // loads of all chunks are independent, so they are issued together
     float4 acc0 = make_float4(0.f, 0.f, 0.f, 0.f), acc1 = acc0;
     const int d0 = 4 * lane, d1 = 4 * lane + 128;
-    for (int s = 0; s < p.num_splits; ++s) {
-        const float ls = __ldg(p.lse_part + s * NH + row);
-        if (ls == -INFINITY)
-            continue;
-        const float w = expf(ls - M);
-        Z += w;
+#pragma unroll 4
+    for (int s = 0; s < S; ++s) {
+        float w = __shfl_sync(0xffffffffu, w_lane, s & 31);
+        if (s >= 32) {
+            const float l2 = __ldg(p.lse_part + s * NH + row);
+            w = l2 == -INFINITY ? 0.f : expf(l2 - M);
+        }
         const float *o = p.o_part + (s * NH + row) * D;
         if (d0 < D) {
             const float4 v = __ldg(reinterpret_cast<const float4 *>(o + d0));
@@ -67,14 +86,12 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergePara
         }
     }
     const float inv = 1.f / Z;
-    if (d0 < D) {
-        uint2 pk = make_uint2(pack_bf16(acc0.x * inv, acc0.y * inv), pack_bf16(acc0.z * inv, acc0.w * inv));
-        *reinterpret_cast<uint2 *>(out + d0) = pk;
-    }
-    if (d1 < D) {
-        uint2 pk = make_uint2(pack_bf16(acc1.x * inv, acc1.y * inv), pack_bf16(acc1.z * inv, acc1.w * inv));
-        *reinterpret_cast<uint2 *>(out + d1) = pk;
-    }
+    if (d0 < D)
+        *reinterpret_cast<uint2 *>(out + d0) =
+            make_uint2(pack_bf16(acc0.x * inv, acc0.y * inv), pack_bf16(acc0.z * inv, acc0.w * inv));
+    if (d1 < D)
+        *reinterpret_cast<uint2 *>(out + d1) =
+            make_uint2(pack_bf16(acc1.x * inv, acc1.y * inv), pack_bf16(acc1.z * inv, acc1.w * inv));
     if (lane == 0 && p.lse_out)
         p.lse_out[row] = M + logf(Z);
 }
@@ -85,8 +102,20 @@ cudaError_t launch_merge(const MergeParams &p, cudaStream_t stream)
 {
     const int64_t rows = static_cast<int64_t>(p.n) * p.num_heads;
     const int64_t blocks = (rows + kMergeWarps - 1) / kMergeWarps;
-    merge_kernel<<<static_cast<unsigned>(blocks), kMergeWarps * 32, 0, stream>>>(p);
-    return cudaGetLastError();
+    // Programmatic dependent launch: the merge grid may be scheduled while the
+    // kernel before it on the stream drains; griddepcontrol.wait above orders
+    // the reads.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+    cfg.blockDim = dim3(kMergeWarps * 32);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, merge_kernel, p);
 }
 
 }  // namespace sa

@@ -32,6 +32,8 @@
 // are applied only on tiles that straddle a boundary.
 #include <cuda_bf16.h>
 
+#include <cstdlib>
+
 #include "sa_internal.h"
 #include "sa_ptx.cuh"
 
@@ -50,12 +52,17 @@ __host__ __device__ constexpr uint32_t col_o(int t) { return 256u + 64u * t; }  
 constexpr float kLog2e = 1.44269504088896340736f;
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 of the largest tolerated p
-// Registers: 384 threads x 168 at launch = 64512.  The producer/MMA warpgroup
-// drops to 56 and the two softmax warpgroups rise to 224:
-// 128 * 56 + 256 * 224 = 64512.
+constexpr int kDefaultPolyOf8 = 0;  // measured: MUFU ex2 (64/clk/SM) is not the limit
+// Registers of the one-pass form: setmaxnreg.inc can only hand out what the
+// block was launched with (384 threads x kLaunchRegs) and what other
+// warpgroups gave back; asking for more blocks the warps for ever.  The
+// producer/MMA warpgroup drops to 56 and the softmax warpgroups rise to 224:
+// 128 * 56 + 256 * 224 = 64512 = 384 * 168.
+constexpr uint32_t kLaunchRegs = 168;  // 65536 / 384, rounded down to the allocation unit
 constexpr uint32_t kRegsLow = 56;
 constexpr uint32_t kRegsHigh = 224;
-static_assert(128 * kRegsLow + 256 * kRegsHigh <= kThreads * 168, "register split exceeds the launch allocation");
+static_assert(128 * kRegsLow + 256 * kRegsHigh <= kThreads * kLaunchRegs,
+              "register split exceeds the block's launch allocation");
 constexpr uint32_t kIdescQK = idesc_bf16_f32(BM, BN, 0);       // Q, K both K-major
 constexpr uint32_t kIdescPV = idesc_bf16_f32(BM, kHeadDim, 1);  // V is MN-major (dims contiguous)
 
@@ -81,6 +88,13 @@ __device__ __forceinline__ void kv_coords(const PrefillParams &p, int slot, int 
     c3 = p.dim_token == 3 ? slot : (p.dim_head == 3 ? g : page);
 }
 
+// kPolyOf8: of every 8 pairs of scores, how many take 2^x on the FMA pipe
+// (exp2_poly_x2) instead of the MUFU unit; balances the two pipes.
+// kTwoPass: the softmax reads each S row from TMEM twice (a max pass and an
+// exp pass, 32 columns at a time), so that it needs few registers and the
+// block runs without register rebalancing; otherwise it holds the whole row
+// and the warpgroups rebalance registers with setmaxnreg.
+template <int kPolyOf8, bool kTwoPass>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                    const __grid_constant__ CUtensorMap tmv, const PrefillParams p)
@@ -144,8 +158,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
 
-    if (warp < 4) {
-        regs_dec<kRegsLow>();
+    if constexpr (!kTwoPass) {
+        if (warp < 4)
+            regs_dec<kRegsLow>();
     }
     if (warp == 0) {
         // ============================ producer ============================
@@ -193,20 +208,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         // ============================ MMA issuer ==========================
-        const uint32_t qaddr[2] = {smem_u32(sm.q[0]), smem_u32(sm.q[1])};
+        // Descriptor bases; a K step adds to the start-address field (bytes >> 4):
+        // 32 bytes (16 dims) for Q/K, 2048 bytes (16 keys) for V.
+        const uint64_t dq0 = smem_desc_sw128(smem_u32(sm.q[0]), 16, 1024);
+        const uint64_t dk0 = smem_desc_sw128(smem_u32(sm.k[0]), 16, 1024);
+        const uint64_t dv0 = smem_desc_sw128(smem_u32(sm.v[0]), 16, 1024);
+        const uint64_t stage_step = kTileBytes >> 4;
         auto issue_qk = [&](int t, int stage) {
-            const uint32_t ka = smem_u32(sm.k[stage]);
+            const uint64_t dq = dq0 + static_cast<uint64_t>(t) * stage_step;  // q[1] follows q[0]
+            const uint64_t dk = dk0 + static_cast<uint64_t>(stage) * stage_step;
 #pragma unroll
-            for (int ks = 0; ks < kHeadDim / 16; ++ks)  // K = 16 dims (32 bytes) per instruction
-                umma_ss(tmem + col_s(t), smem_desc_sw128(qaddr[t] + 32 * ks, 16, 1024),
-                        smem_desc_sw128(ka + 32 * ks, 16, 1024), kIdescQK, ks > 0 ? 1u : 0u);
+            for (int ks = 0; ks < kHeadDim / 16; ++ks)
+                umma_ss(tmem + col_s(t), dq + 2 * ks, dk + 2 * ks, kIdescQK, ks > 0 ? 1u : 0u);
         };
         auto issue_pv = [&](int t, int stage, bool accumulate) {
-            const uint32_t va = smem_u32(sm.v[stage]);
+            const uint64_t dv = dv0 + static_cast<uint64_t>(stage) * stage_step;
 #pragma unroll
             for (int kk = 0; kk < BN / 16; ++kk)  // K = 16 keys: 8 TMEM columns of P, 2 KB of V
-                umma_ts(tmem + col_o(t), tmem + col_s(t) + 8 * kk, smem_desc_sw128(va + 2048 * kk, 16, 1024),
-                        kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
+                umma_ts(tmem + col_o(t), tmem + col_s(t) + 8 * kk, dv + 128 * kk, kIdescPV,
+                        (accumulate || kk > 0) ? 1u : 0u);
         };
         bool ok = mbar_wait(&sm.q_full, 0, p.status) && mbar_wait(&sm.k_full[0], 0, p.status);
         if (ok) {
@@ -267,7 +287,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp >= 4) {
         // ============================ softmax =============================
-        regs_inc<kRegsHigh>();
+        if constexpr (!kTwoPass)
+            regs_inc<kRegsHigh>();
         const int t = (warp - 4) >> 2;
         if (t < NH) {
         const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
@@ -290,60 +311,115 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after();
-            uint32_t sr[4][32];
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-                tmem_ld32(s_addr + 32 * c, sr[c]);
-            tmem_ld_wait();
             const int key0 = (j_first + it) * BN;
             const bool edge =
                 key0 + BN - 1 > p_first || (p.window > 0 && key0 <= p_last - p.window) || key0 + BN > Lkv;
-            float mt = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
+            // hidden keys become -inf (a select: NaN scores past the sequence vanish too)
+            auto mask_chunk = [&](uint32_t *v, int c) {
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
-                    float s = __uint_as_float(sr[c][i]) * p.score_scale;
-                    if (edge) {
-                        const int key = key0 + 32 * c + i;
-                        const bool vis = key <= pos && key < Lkv && (p.window <= 0 || key > pos - p.window);
-                        s = vis ? s : -INFINITY;
-                    }
-                    sr[c][i] = __float_as_uint(s);
-                    mt = fmaxf(mt, s);
+                    const int key = key0 + 32 * c + i;
+                    const bool vis = key <= pos && key < Lkv && (p.window <= 0 || key > pos - p.window);
+                    v[i] = vis ? v[i] : 0xff800000u;
                 }
+            };
+            // row max of the raw scores (score_scale > 0), four independent chains
+            float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+            auto max_chunk = [&](const uint32_t *v) {
+#pragma unroll
+                for (int i = 0; i < 32; i += 8)
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4)
+                        mx[q4] = max3f(mx[q4], __uint_as_float(v[i + 2 * q4]), __uint_as_float(v[i + 2 * q4 + 1]));
+            };
+            uint32_t sr[kTwoPass ? 1 : 4][32];
+            if constexpr (kTwoPass) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    tmem_ld32(s_addr + 32 * c, sr[0]);
+                    tmem_ld_wait();
+                    if (edge)
+                        mask_chunk(sr[0], c);
+                    max_chunk(sr[0]);
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    tmem_ld32(s_addr + 32 * c, sr[c]);
+                tmem_ld_wait();
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    if (edge)
+                        mask_chunk(sr[c], c);
+                    max_chunk(sr[c]);
+                }
+            }
+            const float mt = max3f(mx[0], mx[1], fmaxf(mx[2], mx[3])) * p.score_scale;
             const bool upd = mt > m + kRescaleThreshold;
-            if (__any_sync(0xffffffffu, upd)) {
-                const float mn = upd ? mt : m;
-                const float alpha = upd ? ex2(m - mn) : 1.f;
+            const bool any_upd = __any_sync(0xffffffffu, upd);
+            float alpha = 1.f;
+            if (upd) {
+                alpha = ex2(m - mt);  // m = -inf gives 0
                 l *= alpha;
-                if (it > 0) {  // O holds earlier tiles: bring it to the new max
-#pragma unroll
-                    for (int c = 0; c < 2; ++c) {
-                        uint32_t ov[32];
-                        tmem_ld32(o_addr + 32 * c, ov);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-                        tmem_st32(o_addr + 32 * c, ov);
-                    }
-                }
-                m = mn;
+                m = mt;
             }
             const float mu = m == -INFINITY ? 0.f : m;
-            uint32_t pk[2][32];
+            const float scale = p.score_scale;
+            const float negmu = -mu;
+            // p = 2^(s * scale - m): one FFMA and one MUFU ex2 per score; four
+            // independent partial sums; each 32-score chunk is packed to bf16
+            // and stored as P at once (columns [16c, 16c+16) of S, already read)
+            float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
+            for (int c = 0; c < 4; ++c) {
+                const int cs = kTwoPass ? 0 : c;  // which register chunk holds columns [32c, 32c+32)
+                if constexpr (kTwoPass) {
+                    tmem_ld32(s_addr + 32 * c, sr[0]);
+                    tmem_ld_wait();
+                    if (edge)
+                        mask_chunk(sr[0], c);
+                }
+                uint32_t pk[16];
 #pragma unroll
                 for (int i = 0; i < 32; i += 2) {
-                    const float p0 = ex2(__uint_as_float(sr[c][i]) - mu);
-                    const float p1 = ex2(__uint_as_float(sr[c][i + 1]) - mu);
-                    l += p0 + p1;
-                    pk[c >> 1][(c & 1) * 16 + (i >> 1)] = pack_bf16(p0, p1);
+                    float p0, p1;
+                    if ((((c * 32 + i) >> 1) & 7) < kPolyOf8) {
+                        float x0, x1;
+                        f2_unpack(exp2_poly_x2(f2_pack(fmaf(__uint_as_float(sr[cs][i]), scale, negmu),
+                                                       fmaf(__uint_as_float(sr[cs][i + 1]), scale, negmu))),
+                                  x0, x1);
+                        p0 = x0;
+                        p1 = x1;
+                    } else {
+                        p0 = ex2(fmaf(__uint_as_float(sr[cs][i]), scale, negmu));
+                        p1 = ex2(fmaf(__uint_as_float(sr[cs][i + 1]), scale, negmu));
+                    }
+                    if (edge) {  // hidden keys give exactly 0
+                        p0 = sr[cs][i] == 0xff800000u ? 0.f : p0;
+                        p1 = sr[cs][i + 1] == 0xff800000u ? 0.f : p1;
+                    }
+                    ls[(i >> 1) & 3] += p0 + p1;
+                    pk[i >> 1] = pack_bf16(p0, p1);
                 }
-            tmem_st32(s_addr, pk[0]);  // P overwrites the first 64 columns of S
-            tmem_st32(s_addr + 32, pk[1]);
+                tmem_st16(s_addr + 16 * c, pk);
+            }
+            l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+            if (any_upd && it > 0) {
+                // O holds earlier tiles at the old max: rescale it (after P, when
+                // the scores no longer occupy registers; PV of this tile waits
+                // for p_full below, and PV of the last tile completed before
+                // S of this one was reported)
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t ov[32];
+                    tmem_ld32(o_addr + 32 * c, ov);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+                    tmem_st32(o_addr + 32 * c, ov);
+                }
+            }
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
@@ -390,6 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 size_t prefill_smem_bytes() { return sizeof(PrefillSmem) + 1024; }
 
+template <int kPolyOf8, bool kTwoPass>
 cudaError_t prepare_prefill()
 {
     static int done[64] = {0};
@@ -399,11 +476,32 @@ cudaError_t prepare_prefill()
         return e;
     if (dev >= 0 && dev < 64 && done[dev])
         return cudaSuccess;
-    e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if constexpr (!kTwoPass) {
+        // the setmaxnreg split needs the full launch allocation (see kLaunchRegs)
+        cudaFuncAttributes fa;
+        e = cudaFuncGetAttributes(&fa, prefill_kernel<kPolyOf8, kTwoPass>);
+        if (e != cudaSuccess)
+            return e;
+        if (static_cast<uint32_t>(fa.numRegs) < kLaunchRegs)
+            return cudaErrorInvalidConfiguration;
+    }
+    e = cudaFuncSetAttribute(prefill_kernel<kPolyOf8, kTwoPass>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(prefill_smem_bytes()));
     if (e == cudaSuccess && dev >= 0 && dev < 64)
         done[dev] = 1;
     return e;
+}
+
+template <int kPolyOf8, bool kTwoPass>
+cudaError_t launch_variant(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                           const PrefillParams &p, cudaStream_t stream)
+{
+    cudaError_t e = prepare_prefill<kPolyOf8, kTwoPass>();
+    if (e != cudaSuccess)
+        return e;
+    const dim3 grid(p.num_qo_heads / p.heads_per_cta, p.num_q_tiles, p.batch);
+    prefill_kernel<kPolyOf8, kTwoPass><<<grid, kThreads, prefill_smem_bytes(), stream>>>(tq, tk, tv, p);
+    return cudaGetLastError();
 }
 
 }  // namespace
@@ -411,12 +509,21 @@ cudaError_t prepare_prefill()
 cudaError_t launch_prefill(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                            const PrefillParams &p, cudaStream_t stream)
 {
-    cudaError_t e = prepare_prefill();
-    if (e != cudaSuccess)
-        return e;
-    const dim3 grid(p.num_qo_heads / p.heads_per_cta, p.num_q_tiles, p.batch);
-    prefill_kernel<<<grid, kThreads, prefill_smem_bytes(), stream>>>(tq, tk, tv, p);
-    return cudaGetLastError();
+    // Tuning knobs (the defaults are the measured best):
+    //   SA_PREFILL_POLY (0 or 3): pairs of every 8 whose exp2 runs on the FMA pipe
+    //   SA_PREFILL_ONEPASS=1: hold the S row in registers (setmaxnreg split)
+    static const int poly = [] {
+        const char *v = std::getenv("SA_PREFILL_POLY");
+        return v && *v ? std::atoi(v) : kDefaultPolyOf8;
+    }();
+    static const bool onepass = [] {
+        const char *v = std::getenv("SA_PREFILL_ONEPASS");
+        return v && *v == '1';
+    }();
+    if (onepass)
+        return poly == 3 ? launch_variant<3, false>(tq, tk, tv, p, stream)
+                         : launch_variant<0, false>(tq, tk, tv, p, stream);
+    return poly == 3 ? launch_variant<3, true>(tq, tk, tv, p, stream) : launch_variant<0, true>(tq, tk, tv, p, stream);
 }
 
 }  // namespace sa

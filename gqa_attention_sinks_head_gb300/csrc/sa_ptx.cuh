@@ -64,23 +64,41 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
+// As mbar_try_wait, but the thread may sleep up to `hint_ns` waiting for the
+// phase (it wakes as soon as the phase completes).
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t hint_ns)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for the phase with the given parity to complete.  Returns false when
-// the wait ran out its time limit or another block already recorded a timeout
-// (the status word then holds SA_DEVICE_TIMEOUT).
+// the wait ran out its time limit, or when it has lasted over a millisecond and
+// another block already recorded a timeout (the status word then holds
+// SA_DEVICE_TIMEOUT).  A normal wait touches no global memory: the status word
+// is read only after the first millisecond.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t *status)
 {
     if (mbar_try_wait(bar, parity))
         return true;
     const unsigned long long t0 = global_timer_ns();
     for (;;) {
-        if (mbar_try_wait(bar, parity))
+        if (mbar_try_wait_sleep(bar, parity, 20000u))
             return true;
-        if (*reinterpret_cast<volatile uint32_t *>(status) & SA_DEVICE_TIMEOUT)
-            return false;
-        if (global_timer_ns() - t0 > kWaitLimitNs) {
+        const unsigned long long dt = global_timer_ns() - t0;
+        if (dt > kWaitLimitNs) {
             atomicOr(status, SA_DEVICE_TIMEOUT);
             return false;
         }
+        if (dt > 1000000ull && (*reinterpret_cast<volatile uint32_t *>(status) & SA_DEVICE_TIMEOUT))
+            return false;
     }
 }
 
@@ -320,6 +338,16 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32])
         : "r"(taddr));
 }
 
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t *r)
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32])
 {
     asm volatile(
@@ -333,8 +361,77 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
         : "memory");
 }
 
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// ---------------------------------------------------------- packed fp32 x2
+// Blackwell issues two fp32 adds / fmas per instruction on a 64-bit register pair.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float &lo, float &hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("add.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ float max3f(float a, float b, float c)
+{
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// 2^x for a pair, on the FMA pipe instead of the MUFU unit.  Range reduction:
+// adding 1.5 * 2^23 rounds x to the nearest integer k in the low mantissa bits
+// of t (round to nearest even), so f = x - k lies in [-1/2, 1/2]; a degree-3
+// polynomial gives 2^f; k is added to the exponent field.  The coefficients
+// are a minimax fit of 2^f on [-1/2, 1/2] in relative error, computed for
+// this library by Remez exchange (max relative error 7.5e-5, about 2^-13.7,
+// far below the bf16 rounding of P).  x is clamped at -126 so the exponent
+// cannot wrap: below that the result is a value under 2^-125, i.e. zero for
+// every use here.  (t's bits shifted left by 23 equal k << 23 modulo 2^32,
+// because the bits of 1.5 * 2^23 all shift out.)
+__device__ __forceinline__ uint64_t exp2_poly_x2(uint64_t x)
+{
+    float x0, x1;
+    f2_unpack(x, x0, x1);
+    const uint64_t xc = f2_pack(fmaxf(x0, -126.f), fmaxf(x1, -126.f));
+    const uint64_t t = f2_add(xc, f2_pack(12582912.f, 12582912.f));
+    const uint64_t k = f2_add(t, f2_pack(-12582912.f, -12582912.f));
+    const uint64_t f = f2_fma(k, f2_pack(-1.f, -1.f), xc);
+    uint64_t p = f2_fma(f2_pack(0.0551716685f, 0.0551716685f), f, f2_pack(0.242611125f, 0.242611125f));
+    p = f2_fma(p, f, f2_pack(0.693260968f, 0.693260968f));
+    p = f2_fma(p, f, f2_pack(0.999928057f, 0.999928057f));
+    float p0, p1, t0, t1;
+    f2_unpack(p, p0, p1);
+    f2_unpack(t, t0, t1);
+    return f2_pack(__uint_as_float(__float_as_uint(p0) + (__float_as_uint(t0) << 23)),
+                   __uint_as_float(__float_as_uint(p1) + (__float_as_uint(t1) << 23)));
+}
 
 // Shared-memory matrix descriptor (tcgen05): start address, leading and
 // stride byte offsets (all >> 4), the fixed 0b001 at bits 46-48 and the

@@ -218,7 +218,7 @@ sa_status_t sa_merge_states(const float *o_part, const float *lse_part, int32_t 
  *                the queries' own keys included
  *   seqlens_kv   device int32 [batch]: keys of sequence b (L_kv,b >= L_q,b)
  *   max_q_len, max_kv_len  host upper bounds on the query / key lengths
- *   sinks, window, sm_scale  as sa_decode
+ *   sinks, window as sa_decode; sm_scale > 0 (SA_ERR_UNSUPPORTED otherwise)
  *   out          device bf16 [total_q, num_qo_heads, 64]
  *   lse          device fp32 [total_q, num_qo_heads] or NULL
  * Query i of sequence b sits at position L_kv,b - L_q,b + i (bottom-right aligned).
