@@ -1,25 +1,30 @@
 // prefill.cu -- causal / sliding-window sink-attention prefill on tcgen05.
 //
 // One thread block per (128-query tile, pair of query heads of one kv group,
-// sequence).  The two heads share every K/V tile: the block streams 128-key
-// tiles of K and V through a 3-stage shared-memory ring filled by TMA (16-key
-// boxes, so a paged cache needs no special case), and both heads' products run
-// on the 5th-generation tensor cores with their accumulators in tensor memory:
+// sequence), two blocks per SM.  The two heads share every K/V tile: the block
+// streams 64-key tiles of K and V through a 4-stage shared-memory ring filled
+// by TMA (16-key boxes, so a paged cache needs no special case), and both
+// heads' products run on the 5th-generation tensor cores with their
+// accumulators in tensor memory (256 columns per block):
 //
-//   TMEM columns   0..127  S_0 = Q_0 K^T (fp32), its first 64 columns reused for P_0 (bf16 pairs)
-//                128..255  S_1 / P_1
-//                256..319  O_0 (fp32)      320..383  O_1
+//   TMEM columns   0..63   S_0 = Q_0 K^T (fp32), its first 32 columns reused for P_0 (bf16 pairs)
+//                 64..127  O_0 (fp32)
+//                128..191  S_1 / P_1       192..255  O_1
 //
-// Warp roles (384 threads):
+// Warp roles (320 threads):
 //   warp 0      producer: Q tiles once, then K and V tiles (page-table walk, TMA)
 //   warp 1      MMA issuer: S_t = Q_t K^T (SS form), O_t += P_t V (P from TMEM, TS form);
 //               also zeroes the rows of the last V tile that lie past the sequence
-//   warps 4-7   softmax of head 0, warps 8-11 softmax of head 1 (one thread per query row)
+//   warps 2-5   softmax of head 0, warps 6-9 softmax of head 1: one thread per query
+//               row; warp w reads TMEM lanes 32*(w%4) .. +31, so each group of four
+//               warps covers all 128 rows
 //
-// Per key tile the MMA warp issues, for each head t: PV_t(j) once P_t(j) is in
-// TMEM, then at once QK_t(j+1).  The tensor pipe runs a thread's MMAs in
-// order, so the commit that reports S_t(j+1) also proves that PV_t(j) read
-// P_t(j) and finished writing O_t; the softmax may then rescale O_t.
+// Two blocks per SM give four independent softmax streams per SM, and one
+// block's prologue, tail and epilogue overlap the other block's work.  Per key
+// tile the MMA warp issues, for each head t: PV_t(j) once P_t(j) is in TMEM,
+// then at once QK_t(j+1).  The tensor pipe runs a thread's MMAs in order, so
+// the commit that reports S_t(j+1) also proves that PV_t(j) read P_t(j) and
+// finished writing O_t; the softmax may then rescale O_t.
 //
 // Softmax ("GPT-OSS on day 0" (Perplexity), section "Sink Attention"): each
 // row keeps a running max m (base 2) and sum l, started at the head's sink
@@ -32,8 +37,6 @@
 // are applied only on tiles that straddle a boundary.
 #include <cuda_bf16.h>
 
-#include <cstdlib>
-
 #include "sa_internal.h"
 #include "sa_ptx.cuh"
 
@@ -41,35 +44,26 @@ namespace sa {
 namespace {
 
 constexpr int BM = 128;  // query rows per tile
-constexpr int BN = 128;  // keys per tile
-constexpr int kStages = 3;
-constexpr int kThreads = 384;
-constexpr uint32_t kTileBytes = BN * kHeadDim * 2;  // 16 KB
-constexpr uint32_t kBoxBytes = 16 * kHeadDim * 2;   // one 16-key box
-constexpr uint32_t kTmemCols = 512;
-__host__ __device__ constexpr uint32_t col_s(int t) { return 128u * t; }         // S_t / P_t
-__host__ __device__ constexpr uint32_t col_o(int t) { return 256u + 64u * t; }   // O_t
+constexpr int BN = 64;   // keys per tile
+constexpr int kStages = 4;
+constexpr int kThreads = 320;
+constexpr int kFirstSoftmaxWarp = 2;
+constexpr uint32_t kQTileBytes = BM * kHeadDim * 2;   // 16 KB
+constexpr uint32_t kKVTileBytes = BN * kHeadDim * 2;  // 8 KB
+constexpr uint32_t kBoxBytes = 16 * kHeadDim * 2;     // one 16-key box
+constexpr uint32_t kTmemCols = 256;
+__host__ __device__ constexpr uint32_t col_s(int t) { return 128u * t; }        // S_t / P_t
+__host__ __device__ constexpr uint32_t col_o(int t) { return 128u * t + 64u; }  // O_t
 constexpr float kLog2e = 1.44269504088896340736f;
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 of the largest tolerated p
-constexpr int kDefaultPolyOf8 = 0;  // measured: MUFU ex2 (64/clk/SM) is not the limit
-// Registers of the one-pass form: setmaxnreg.inc can only hand out what the
-// block was launched with (384 threads x kLaunchRegs) and what other
-// warpgroups gave back; asking for more blocks the warps for ever.  The
-// producer/MMA warpgroup drops to 56 and the softmax warpgroups rise to 224:
-// 128 * 56 + 256 * 224 = 64512 = 384 * 168.
-constexpr uint32_t kLaunchRegs = 168;  // 65536 / 384, rounded down to the allocation unit
-constexpr uint32_t kRegsLow = 56;
-constexpr uint32_t kRegsHigh = 224;
-static_assert(128 * kRegsLow + 256 * kRegsHigh <= kThreads * kLaunchRegs,
-              "register split exceeds the block's launch allocation");
-constexpr uint32_t kIdescQK = idesc_bf16_f32(BM, BN, 0);       // Q, K both K-major
+constexpr uint32_t kIdescQK = idesc_bf16_f32(BM, BN, 0);        // Q, K both K-major
 constexpr uint32_t kIdescPV = idesc_bf16_f32(BM, kHeadDim, 1);  // V is MN-major (dims contiguous)
 
 struct PrefillSmem {
-    uint8_t q[2][kTileBytes];
-    uint8_t k[kStages][kTileBytes];
-    uint8_t v[kStages][kTileBytes];
+    uint8_t q[2][kQTileBytes];
+    uint8_t k[kStages][kKVTileBytes];
+    uint8_t v[kStages][kKVTileBytes];
     uint64_t q_full;
     uint64_t k_full[kStages];
     uint64_t v_full[kStages];
@@ -79,6 +73,7 @@ struct PrefillSmem {
     uint64_t o_done[2];
     uint32_t tmem_base;
 };
+static_assert(sizeof(PrefillSmem) + 1024 <= 113 * 1024, "two blocks must fit one SM's shared memory");
 
 __device__ __forceinline__ void kv_coords(const PrefillParams &p, int slot, int g, int page, int &c1, int &c2,
                                           int &c3)
@@ -88,14 +83,100 @@ __device__ __forceinline__ void kv_coords(const PrefillParams &p, int slot, int 
     c3 = p.dim_token == 3 ? slot : (p.dim_head == 3 ? g : page);
 }
 
-// kPolyOf8: of every 8 pairs of scores, how many take 2^x on the FMA pipe
-// (exp2_poly_x2) instead of the MUFU unit; balances the two pipes.
-// kTwoPass: the softmax reads each S row from TMEM twice (a max pass and an
-// exp pass, 32 columns at a time), so that it needs few registers and the
-// block runs without register rebalancing; otherwise it holds the whole row
-// and the warpgroups rebalance registers with setmaxnreg.
-template <int kPolyOf8, bool kTwoPass>
-__global__ void __launch_bounds__(kThreads, 1)
+// Edge tiles (straddling the causal diagonal, the window's lower edge or the
+// sequence end): overwrite the hidden keys' scores in TMEM with -inf, by
+// select, so that NaN scores past the sequence vanish too.  Interior tiles
+// skip this and the softmax body carries no mask arithmetic.
+__device__ __forceinline__ void mask_tile(uint32_t s_addr, int key0, int pos, int Lkv, int window)
+{
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(s_addr + 32 * c, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const int key = key0 + 32 * c + i;
+            const bool vis = key <= pos && key < Lkv && (window <= 0 || key > pos - window);
+            v[i] = vis ? v[i] : 0xff800000u;
+        }
+        tmem_st32(s_addr + 32 * c, v);
+    }
+    tmem_st_wait();
+}
+
+// One 64-key tile of the online softmax for the query row this thread owns.
+// Pass 1 reads S (TMEM) 16 columns at a time for the row max; pass 2 reads it
+// again, forms p = 2^(s*scale - m) (fma.f32x2, ex2; ex2 of -inf is exactly 0),
+// adds p into two paired sums (add.f32x2), packs p to bf16 and stores it as P
+// over the leading columns of S.  When m moved, O is rescaled.
+__device__ __forceinline__ void softmax_tile(uint32_t s_addr, uint32_t o_addr, float scale, bool o_live, float &m,
+                                             float &l)
+{
+    constexpr int kChunk = 16;  // columns per TMEM read: few live registers at two blocks per SM
+    uint32_t sr[kChunk];
+    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+    for (int c = 0; c < BN / kChunk; ++c) {
+        tmem_ld16(s_addr + kChunk * c, sr);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < kChunk; i += 8)
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4)
+                mx[q4] = max3f(mx[q4], __uint_as_float(sr[i + 2 * q4]), __uint_as_float(sr[i + 2 * q4 + 1]));
+    }
+    const float mt = max3f(mx[0], mx[1], fmaxf(mx[2], mx[3])) * scale;  // scale > 0
+    const bool upd = mt > m + kRescaleThreshold;
+    const bool any_upd = __any_sync(0xffffffffu, upd);
+    float alpha = 1.f;
+    if (upd) {
+        alpha = ex2(m - mt);  // m = -inf gives 0
+        l *= alpha;
+        m = mt;
+    }
+    const float negmu = m == -INFINITY ? 0.f : -m;
+    const uint64_t scale2 = f2_pack(scale, scale);
+    const uint64_t negmu2 = f2_pack(negmu, negmu);
+    uint64_t ls2[2] = {0ull, 0ull};
+#pragma unroll
+    for (int c = 0; c < BN / kChunk; ++c) {
+        tmem_ld16(s_addr + kChunk * c, sr);
+        tmem_ld_wait();
+        uint32_t pk[kChunk / 2];
+#pragma unroll
+        for (int i = 0; i < kChunk; i += 2) {
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[i]), __uint_as_float(sr[i + 1])), scale2, negmu2), x0, x1);
+            const float p0 = ex2(x0);
+            const float p1 = ex2(x1);
+            ls2[(i >> 1) & 1] = f2_add(ls2[(i >> 1) & 1], f2_pack(p0, p1));
+            pk[i >> 1] = pack_bf16(p0, p1);
+        }
+        tmem_st8(s_addr + (kChunk / 2) * c, pk);  // P columns [8c, 8c+8): S columns already read
+    }
+    float a0, a1, b0, b1;
+    f2_unpack(ls2[0], a0, a1);
+    f2_unpack(ls2[1], b0, b1);
+    l += (a0 + a1) + (b0 + b1);
+    if (any_upd && o_live) {
+        // O holds earlier tiles at the old max: rescale it.  PV of this tile
+        // waits for the P handshake, and PV of the previous tile completed
+        // before this S was reported.
+#pragma unroll
+        for (int c = 0; c < kHeadDim / 32; ++c) {
+            uint32_t ov[32];
+            tmem_ld32(o_addr + 32 * c, ov);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+            tmem_st32(o_addr + 32 * c, ov);
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 2)
     prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                    const __grid_constant__ CUtensorMap tmv, const PrefillParams p)
 {
@@ -128,7 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (q0 >= Lq)
         return;
     const int rows = min(BM, Lq - q0);
-    const int off = Lkv - Lq;                 // query i sits at position off + i
+    const int off = Lkv - Lq;  // query i sits at position off + i
     const int p_first = off + q0;
     const int p_last = off + q0 + rows - 1;
     const int k_lo = p.window > 0 ? max(0, p_first - p.window + 1) : 0;
@@ -158,17 +239,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
 
-    if constexpr (!kTwoPass) {
-        if (warp < 4)
-            regs_dec<kRegsLow>();
-    }
     if (warp == 0) {
         // ============================ producer ============================
         if (lane == 0) {
             tma_prefetch_desc(&tmq);
             tma_prefetch_desc(&tmk);
             tma_prefetch_desc(&tmv);
-            mbar_arrive_expect_tx(&sm.q_full, static_cast<uint32_t>(NH) * kTileBytes);
+            mbar_arrive_expect_tx(&sm.q_full, static_cast<uint32_t>(NH) * kQTileBytes);
             for (int t = 0; t < NH; ++t)
                 tma_load_3d(sm.q[t], &tmq, &sm.q_full, 0, h0 + t, q_beg + q0);
         }
@@ -213,16 +290,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t dq0 = smem_desc_sw128(smem_u32(sm.q[0]), 16, 1024);
         const uint64_t dk0 = smem_desc_sw128(smem_u32(sm.k[0]), 16, 1024);
         const uint64_t dv0 = smem_desc_sw128(smem_u32(sm.v[0]), 16, 1024);
-        const uint64_t stage_step = kTileBytes >> 4;
         auto issue_qk = [&](int t, int stage) {
-            const uint64_t dq = dq0 + static_cast<uint64_t>(t) * stage_step;  // q[1] follows q[0]
-            const uint64_t dk = dk0 + static_cast<uint64_t>(stage) * stage_step;
+            const uint64_t dq = dq0 + static_cast<uint64_t>(t) * (kQTileBytes >> 4);  // q[1] follows q[0]
+            const uint64_t dk = dk0 + static_cast<uint64_t>(stage) * (kKVTileBytes >> 4);
 #pragma unroll
             for (int ks = 0; ks < kHeadDim / 16; ++ks)
                 umma_ss(tmem + col_s(t), dq + 2 * ks, dk + 2 * ks, kIdescQK, ks > 0 ? 1u : 0u);
         };
         auto issue_pv = [&](int t, int stage, bool accumulate) {
-            const uint64_t dv = dv0 + static_cast<uint64_t>(stage) * stage_step;
+            const uint64_t dv = dv0 + static_cast<uint64_t>(stage) * (kKVTileBytes >> 4);
 #pragma unroll
             for (int kk = 0; kk < BN / 16; ++kk)  // K = 16 keys: 8 TMEM columns of P, 2 KB of V
                 umma_ts(tmem + col_o(t), tmem + col_s(t) + 8 * kk, dv + 128 * kk, kIdescPV,
@@ -285,12 +361,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int t = 0; t < NH; ++t)
                 umma_commit(&sm.o_done[t]);
         __syncwarp();
-    } else if (warp >= 4) {
+    } else if (((warp - kFirstSoftmaxWarp) >> 2) < NH) {
         // ============================ softmax =============================
-        if constexpr (!kTwoPass)
-            regs_inc<kRegsHigh>();
-        const int t = (warp - 4) >> 2;
-        if (t < NH) {
+        const int t = (warp - kFirstSoftmaxWarp) >> 2;
         const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
         const int row = quarter * 32 + lane;
         const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
@@ -314,112 +387,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int key0 = (j_first + it) * BN;
             const bool edge =
                 key0 + BN - 1 > p_first || (p.window > 0 && key0 <= p_last - p.window) || key0 + BN > Lkv;
-            // hidden keys become -inf (a select: NaN scores past the sequence vanish too)
-            auto mask_chunk = [&](uint32_t *v, int c) {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int key = key0 + 32 * c + i;
-                    const bool vis = key <= pos && key < Lkv && (p.window <= 0 || key > pos - p.window);
-                    v[i] = vis ? v[i] : 0xff800000u;
-                }
-            };
-            // row max of the raw scores (score_scale > 0), four independent chains
-            float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-            auto max_chunk = [&](const uint32_t *v) {
-#pragma unroll
-                for (int i = 0; i < 32; i += 8)
-#pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4)
-                        mx[q4] = max3f(mx[q4], __uint_as_float(v[i + 2 * q4]), __uint_as_float(v[i + 2 * q4 + 1]));
-            };
-            uint32_t sr[kTwoPass ? 1 : 4][32];
-            if constexpr (kTwoPass) {
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    tmem_ld32(s_addr + 32 * c, sr[0]);
-                    tmem_ld_wait();
-                    if (edge)
-                        mask_chunk(sr[0], c);
-                    max_chunk(sr[0]);
-                }
-            } else {
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    tmem_ld32(s_addr + 32 * c, sr[c]);
-                tmem_ld_wait();
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    if (edge)
-                        mask_chunk(sr[c], c);
-                    max_chunk(sr[c]);
-                }
-            }
-            const float mt = max3f(mx[0], mx[1], fmaxf(mx[2], mx[3])) * p.score_scale;
-            const bool upd = mt > m + kRescaleThreshold;
-            const bool any_upd = __any_sync(0xffffffffu, upd);
-            float alpha = 1.f;
-            if (upd) {
-                alpha = ex2(m - mt);  // m = -inf gives 0
-                l *= alpha;
-                m = mt;
-            }
-            const float mu = m == -INFINITY ? 0.f : m;
-            const float scale = p.score_scale;
-            const float negmu = -mu;
-            // p = 2^(s * scale - m): one FFMA and one MUFU ex2 per score; four
-            // independent partial sums; each 32-score chunk is packed to bf16
-            // and stored as P at once (columns [16c, 16c+16) of S, already read)
-            float ls[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const int cs = kTwoPass ? 0 : c;  // which register chunk holds columns [32c, 32c+32)
-                if constexpr (kTwoPass) {
-                    tmem_ld32(s_addr + 32 * c, sr[0]);
-                    tmem_ld_wait();
-                    if (edge)
-                        mask_chunk(sr[0], c);
-                }
-                uint32_t pk[16];
-#pragma unroll
-                for (int i = 0; i < 32; i += 2) {
-                    float p0, p1;
-                    if ((((c * 32 + i) >> 1) & 7) < kPolyOf8) {
-                        float x0, x1;
-                        f2_unpack(exp2_poly_x2(f2_pack(fmaf(__uint_as_float(sr[cs][i]), scale, negmu),
-                                                       fmaf(__uint_as_float(sr[cs][i + 1]), scale, negmu))),
-                                  x0, x1);
-                        p0 = x0;
-                        p1 = x1;
-                    } else {
-                        p0 = ex2(fmaf(__uint_as_float(sr[cs][i]), scale, negmu));
-                        p1 = ex2(fmaf(__uint_as_float(sr[cs][i + 1]), scale, negmu));
-                    }
-                    if (edge) {  // hidden keys give exactly 0
-                        p0 = sr[cs][i] == 0xff800000u ? 0.f : p0;
-                        p1 = sr[cs][i + 1] == 0xff800000u ? 0.f : p1;
-                    }
-                    ls[(i >> 1) & 3] += p0 + p1;
-                    pk[i >> 1] = pack_bf16(p0, p1);
-                }
-                tmem_st16(s_addr + 16 * c, pk);
-            }
-            l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-            if (any_upd && it > 0) {
-                // O holds earlier tiles at the old max: rescale it (after P, when
-                // the scores no longer occupy registers; PV of this tile waits
-                // for p_full below, and PV of the last tile completed before
-                // S of this one was reported)
-#pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    uint32_t ov[32];
-                    tmem_ld32(o_addr + 32 * c, ov);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-                    tmem_st32(o_addr + 32 * c, ov);
-                }
-            }
+            if (edge)
+                mask_tile(s_addr, key0, pos, Lkv, p.window);
+            softmax_tile(s_addr, o_addr, p.score_scale, it > 0, m, l);
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
@@ -429,29 +399,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---- epilogue: O / l, lse = (m + log2 l) ln 2 ----
         if (ok && mbar_wait(&sm.o_done[t], 0, p.status)) {
             tc_fence_after();
-            uint32_t ov[2][32];
-            tmem_ld32(o_addr, ov[0]);
-            tmem_ld32(o_addr + 32, ov[1]);
-            tmem_ld_wait();
-            if (qi < Lq) {
-                const float inv = l > 0.f ? 1.f / l : 0.f;
-                const int64_t orow = static_cast<int64_t>(q_beg + qi) * p.num_qo_heads + h;
-                uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.out) + orow * kHeadDim);
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const int64_t orow = static_cast<int64_t>(q_beg + qi) * p.num_qo_heads + h;
+            uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.out) + orow * kHeadDim);
 #pragma unroll
-                for (int c = 0; c < 2; ++c)
+            for (int c = 0; c < kHeadDim / 32; ++c) {  // 32 columns of O at a time
+                uint32_t ov[32];
+                tmem_ld32(o_addr + 32 * c, ov);
+                tmem_ld_wait();
+                if (qi < Lq) {
 #pragma unroll
                     for (int v4 = 0; v4 < 4; ++v4) {
                         uint4 w;
-                        w.x = pack_bf16(__uint_as_float(ov[c][8 * v4 + 0]) * inv, __uint_as_float(ov[c][8 * v4 + 1]) * inv);
-                        w.y = pack_bf16(__uint_as_float(ov[c][8 * v4 + 2]) * inv, __uint_as_float(ov[c][8 * v4 + 3]) * inv);
-                        w.z = pack_bf16(__uint_as_float(ov[c][8 * v4 + 4]) * inv, __uint_as_float(ov[c][8 * v4 + 5]) * inv);
-                        w.w = pack_bf16(__uint_as_float(ov[c][8 * v4 + 6]) * inv, __uint_as_float(ov[c][8 * v4 + 7]) * inv);
+                        w.x = pack_bf16(__uint_as_float(ov[8 * v4 + 0]) * inv, __uint_as_float(ov[8 * v4 + 1]) * inv);
+                        w.y = pack_bf16(__uint_as_float(ov[8 * v4 + 2]) * inv, __uint_as_float(ov[8 * v4 + 3]) * inv);
+                        w.z = pack_bf16(__uint_as_float(ov[8 * v4 + 4]) * inv, __uint_as_float(ov[8 * v4 + 5]) * inv);
+                        w.w = pack_bf16(__uint_as_float(ov[8 * v4 + 6]) * inv, __uint_as_float(ov[8 * v4 + 7]) * inv);
                         dst[c * 4 + v4] = w;
                     }
-                if (p.lse)
-                    p.lse[orow] = l > 0.f ? (m + lg2(l)) * kLn2 : -INFINITY;
+                }
             }
-        }
+            if (qi < Lq && p.lse)
+                p.lse[orow] = l > 0.f ? (m + lg2(l)) * kLn2 : -INFINITY;
         }
     }
 
@@ -466,7 +435,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 size_t prefill_smem_bytes() { return sizeof(PrefillSmem) + 1024; }
 
-template <int kPolyOf8, bool kTwoPass>
 cudaError_t prepare_prefill()
 {
     static int done[64] = {0};
@@ -476,32 +444,11 @@ cudaError_t prepare_prefill()
         return e;
     if (dev >= 0 && dev < 64 && done[dev])
         return cudaSuccess;
-    if constexpr (!kTwoPass) {
-        // the setmaxnreg split needs the full launch allocation (see kLaunchRegs)
-        cudaFuncAttributes fa;
-        e = cudaFuncGetAttributes(&fa, prefill_kernel<kPolyOf8, kTwoPass>);
-        if (e != cudaSuccess)
-            return e;
-        if (static_cast<uint32_t>(fa.numRegs) < kLaunchRegs)
-            return cudaErrorInvalidConfiguration;
-    }
-    e = cudaFuncSetAttribute(prefill_kernel<kPolyOf8, kTwoPass>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(prefill_smem_bytes()));
     if (e == cudaSuccess && dev >= 0 && dev < 64)
         done[dev] = 1;
     return e;
-}
-
-template <int kPolyOf8, bool kTwoPass>
-cudaError_t launch_variant(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                           const PrefillParams &p, cudaStream_t stream)
-{
-    cudaError_t e = prepare_prefill<kPolyOf8, kTwoPass>();
-    if (e != cudaSuccess)
-        return e;
-    const dim3 grid(p.num_qo_heads / p.heads_per_cta, p.num_q_tiles, p.batch);
-    prefill_kernel<kPolyOf8, kTwoPass><<<grid, kThreads, prefill_smem_bytes(), stream>>>(tq, tk, tv, p);
-    return cudaGetLastError();
 }
 
 }  // namespace
@@ -509,21 +456,12 @@ cudaError_t launch_variant(const CUtensorMap &tq, const CUtensorMap &tk, const C
 cudaError_t launch_prefill(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                            const PrefillParams &p, cudaStream_t stream)
 {
-    // Tuning knobs (the defaults are the measured best):
-    //   SA_PREFILL_POLY (0 or 3): pairs of every 8 whose exp2 runs on the FMA pipe
-    //   SA_PREFILL_ONEPASS=1: hold the S row in registers (setmaxnreg split)
-    static const int poly = [] {
-        const char *v = std::getenv("SA_PREFILL_POLY");
-        return v && *v ? std::atoi(v) : kDefaultPolyOf8;
-    }();
-    static const bool onepass = [] {
-        const char *v = std::getenv("SA_PREFILL_ONEPASS");
-        return v && *v == '1';
-    }();
-    if (onepass)
-        return poly == 3 ? launch_variant<3, false>(tq, tk, tv, p, stream)
-                         : launch_variant<0, false>(tq, tk, tv, p, stream);
-    return poly == 3 ? launch_variant<3, true>(tq, tk, tv, p, stream) : launch_variant<0, true>(tq, tk, tv, p, stream);
+    cudaError_t e = prepare_prefill();
+    if (e != cudaSuccess)
+        return e;
+    const dim3 grid(p.num_qo_heads / p.heads_per_cta, p.num_q_tiles, p.batch);
+    prefill_kernel<<<grid, kThreads, prefill_smem_bytes(), stream>>>(tq, tk, tv, p);
+    return cudaGetLastError();
 }
 
 }  // namespace sa

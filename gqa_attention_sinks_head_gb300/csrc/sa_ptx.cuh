@@ -371,6 +371,13 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
         : "memory");
 }
 
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t *r)
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
+}
+
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
@@ -403,34 +410,6 @@ __device__ __forceinline__ float max3f(float a, float b, float c)
     float d;
     asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
     return d;
-}
-
-// 2^x for a pair, on the FMA pipe instead of the MUFU unit.  Range reduction:
-// adding 1.5 * 2^23 rounds x to the nearest integer k in the low mantissa bits
-// of t (round to nearest even), so f = x - k lies in [-1/2, 1/2]; a degree-3
-// polynomial gives 2^f; k is added to the exponent field.  The coefficients
-// are a minimax fit of 2^f on [-1/2, 1/2] in relative error, computed for
-// this library by Remez exchange (max relative error 7.5e-5, about 2^-13.7,
-// far below the bf16 rounding of P).  x is clamped at -126 so the exponent
-// cannot wrap: below that the result is a value under 2^-125, i.e. zero for
-// every use here.  (t's bits shifted left by 23 equal k << 23 modulo 2^32,
-// because the bits of 1.5 * 2^23 all shift out.)
-__device__ __forceinline__ uint64_t exp2_poly_x2(uint64_t x)
-{
-    float x0, x1;
-    f2_unpack(x, x0, x1);
-    const uint64_t xc = f2_pack(fmaxf(x0, -126.f), fmaxf(x1, -126.f));
-    const uint64_t t = f2_add(xc, f2_pack(12582912.f, 12582912.f));
-    const uint64_t k = f2_add(t, f2_pack(-12582912.f, -12582912.f));
-    const uint64_t f = f2_fma(k, f2_pack(-1.f, -1.f), xc);
-    uint64_t p = f2_fma(f2_pack(0.0551716685f, 0.0551716685f), f, f2_pack(0.242611125f, 0.242611125f));
-    p = f2_fma(p, f, f2_pack(0.693260968f, 0.693260968f));
-    p = f2_fma(p, f, f2_pack(0.999928057f, 0.999928057f));
-    float p0, p1, t0, t1;
-    f2_unpack(p, p0, p1);
-    f2_unpack(t, t0, t1);
-    return f2_pack(__uint_as_float(__float_as_uint(p0) + (__float_as_uint(t0) << 23)),
-                   __uint_as_float(__float_as_uint(p1) + (__float_as_uint(t1) << 23)));
 }
 
 // Shared-memory matrix descriptor (tcgen05): start address, leading and
