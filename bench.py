@@ -236,6 +236,7 @@ class DecodeBench:
         self.step_bytes = sum(cl["bytes"] for cl in self.calls)
         self.kernels_per_step = sum(2 if cl["S"] > 1 else 1 for cl in self.calls)
         self.unit = "GB/s"
+        self.e2e_api = "sa_decode with pinned host q/seqlens/page table in, out/lse back; KV cache resident"
 
     def amount(self):
         return self.step_bytes / 1e9
@@ -351,6 +352,7 @@ class PrefillBench:
         self.kernels_per_step = len(self.calls)
         self.unit = "TFLOP/s"
         self.elem = 2
+        self.e2e_api = "sa_prefill with pinned host q, k, v in, out/lse of both calls back"
         self.B = len(self.q_lens)
         self.maxlen = max(self.kv_lens)
 
@@ -377,13 +379,17 @@ class PrefillBench:
         torch = self.torch
         c = self.case
         hq = torch.empty(c.q.shape, dtype=c.q.dtype, pin_memory=True).copy_(c.q.cpu())
+        hk = torch.empty(c.kv.k.shape, dtype=c.kv.k.dtype, pin_memory=True).copy_(c.kv.k.cpu())
+        hv = torch.empty(c.kv.v.shape, dtype=c.kv.v.dtype, pin_memory=True).copy_(c.kv.v.cpu())
         houts = [(torch.empty(cl["out"].shape, dtype=torch.bfloat16, pin_memory=True),
                   torch.empty(cl["lse"].shape, dtype=torch.float32, pin_memory=True)) for cl in self.calls]
-        h2d = hq.numel() * 2
+        h2d = hq.numel() * 2 + (hk.numel() + hv.numel()) * hk.element_size()
         d2h = sum(o.numel() * 2 + l.numel() * 4 for o, l in houts)
 
         def one():
             c.q.copy_(hq, non_blocking=True)
+            c.kv.k.copy_(hk, non_blocking=True)
+            c.kv.v.copy_(hv, non_blocking=True)
             for cl, (ho, hl) in zip(self.calls, houts):
                 self.run_call(cl, stream)
                 ho.copy_(cl["out"], non_blocking=True)
@@ -499,16 +505,20 @@ def run_native(args, world, rank, local):
                      "frac_of_nominal": round(achieved / nominal, 4)},
         "clocks": clocks,
         "e2e": {"value": round(e2e_value, 2), "unit": wl.unit, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "api": "sa_decode with pinned host q/seqlens/page table in, "
-                                                 "out/lse back; KV cache resident"},
+                "d2h_bytes_per_step": d2h, "api": wl.e2e_api},
         "gpu_launches": steps * wl.kernels_per_step,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
-        dt, nbytes, desc = wl.oracle_sample(30.0)
+        # repeat the sample until about 10 s of host work is timed
+        dt, nbytes, reps = 0.0, 0, 0
+        while dt < 10.0 and reps < 1000:
+            d1, b1, desc = wl.oracle_sample(30.0)
+            dt, nbytes, reps = dt + d1, nbytes + b1, reps + 1
         line["cpu_baseline"] = {"value": round(nbytes / (1e9 if wl.unit == "GB/s" else 1e12) / dt, 6),
                                 "unit": wl.unit,
-                                "cores": oracle.num_threads(), "kind": "oracle", "sample": desc,
+                                "cores": oracle.num_threads(), "kind": "oracle",
+                                "sample": "%s; timed %d times" % (desc, reps),
                                 "seconds": round(dt, 2)}
     if rank == 0:
         print(json.dumps(line), flush=True)
