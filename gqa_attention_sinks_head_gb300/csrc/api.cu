@@ -364,16 +364,10 @@ int sa_version(void) { return SA_VERSION; }
 
 int32_t sa_decode_num_splits(int32_t batch, int32_t num_kv_heads, int32_t max_kv_len, int32_t window)
 {
-    const char *force = std::getenv("SA_FORCE_SPLITS");
-    if (force && *force) {
-        const int v = std::atoi(force);
-        if (v >= 1)
-            return std::min(v, kMaxSplits);
-    }
     int sms = 0, bps = 0;
     if (!device_shape(false, &sms, &bps)) {
         sms = 152;  // no device visible: size for a GB300
-        bps = 3;
+        bps = 4;
     }
     return choose_splits(batch, std::max(1, num_kv_heads), max_kv_len, window, sms, bps);
 }

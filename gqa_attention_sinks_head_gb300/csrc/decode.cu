@@ -9,8 +9,8 @@
 //
 // Pipeline: warp 4 is the producer.  It walks the page table (32 entries
 // prefetched ahead in registers) and issues one TMA tile copy per 16-key page
-// slice of K and of V (2 KB each in bf16, 1 KB in FP8) into a 4-stage ring,
-// completing on an mbarrier with transaction bytes.  Warps 0-3 are consumers:
+// slice of K and of V (2 KB each in bf16, 1 KB in FP8) into a ring of
+// stages, completing on an mbarrier with transaction bytes.  Warps 0-3 are consumers:
 // stage i holds four tiles, one per consumer warp.  The tiles land in shared
 // memory with the TMA 128-byte (bf16) / 64-byte (FP8) swizzle so that the
 // ldmatrix reads below are free of bank conflicts.
@@ -437,16 +437,6 @@ cudaError_t prepare_decode()
     return e;
 }
 
-// SA_DECODE_STAGES (3 or 4): pipeline depth, a tuning knob; default 3.
-int decode_stages()
-{
-    static const int st = [] {
-        const char *v = std::getenv("SA_DECODE_STAGES");
-        return (v && std::atoi(v) == 4) ? 4 : kDefaultStages;
-    }();
-    return st;
-}
-
 template <bool FP8, int kStages>
 cudaError_t occupancy_of(int *blocks_per_sm)
 {
@@ -472,17 +462,13 @@ cudaError_t launch_of(const CUtensorMap &tk, const CUtensorMap &tv, const Decode
 
 cudaError_t decode_occupancy(bool fp8, int *blocks_per_sm)
 {
-    if (decode_stages() == 4)
-        return fp8 ? occupancy_of<true, 8>(blocks_per_sm) : occupancy_of<false, 4>(blocks_per_sm);
-    return fp8 ? occupancy_of<true, 6>(blocks_per_sm) : occupancy_of<false, 3>(blocks_per_sm);
+    return fp8 ? occupancy_of<true, 2 * kDefaultStages>(blocks_per_sm) : occupancy_of<false, kDefaultStages>(blocks_per_sm);
 }
 
 cudaError_t launch_decode(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p, bool fp8,
                           cudaStream_t stream)
 {
-    if (decode_stages() == 4)
-        return fp8 ? launch_of<true, 8>(tk, tv, p, stream) : launch_of<false, 4>(tk, tv, p, stream);
-    return fp8 ? launch_of<true, 6>(tk, tv, p, stream) : launch_of<false, 3>(tk, tv, p, stream);
+    return fp8 ? launch_of<true, 2 * kDefaultStages>(tk, tv, p, stream) : launch_of<false, kDefaultStages>(tk, tv, p, stream);
 }
 
 }  // namespace sa
