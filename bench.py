@@ -34,7 +34,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "sink-attn decode HBM GB/s (% peak); prefill TFLOP/s (% bf16 tensor peak)"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-DEFAULT_STEPS = {1: 2000, 2: 2000, 3: 50, 4: 100, 5: 500}
+DEFAULT_STEPS = {1: 2000, 2: 2000, 3: 50, 4: 100, 5: 500, 6: 50, 7: 50}
 
 
 # ------------------------------------------------------------------ helpers
@@ -192,7 +192,10 @@ def prefill_flops(q_lens, kv_lens, window, hq, dim):
 
 
 def windows_of(cfg):
-    return {1: [0], 2: [0, 128], 3: [0, 128], 4: [0], 5: [0, 128, 0, 128]}[cfg]
+    return {1: [0], 2: [0, 128], 3: [0, 128], 4: [0], 5: [0, 128, 0, 128], 6: [0, 128], 7: [0, 128]}[cfg]
+
+
+PREFILL_CONFIGS = (3, 6, 7)
 
 
 def workload_name(cfg):
@@ -202,6 +205,10 @@ def workload_name(cfg):
         3: "prefill T=8192 causal contiguous bf16, 64q/8kv heads, D=64, step = w=0 call + w=128 call",
         4: "decode B=128 L=32768 paged P=16 bf16 split-KV, 64q/8kv heads, D=64, w=0",
         5: "decode B=256 L=8192 paged P=16 fp8-e4m3, 64q/8kv heads, D=64, step = w=0,128,0,128",
+        6: "chunked prefill B=8, 1024 new queries each on a paged P=16 bf16 context L_kv~U[2048,16384], "
+           "64q/8kv heads, D=64, step = w=0 call + w=128 call",
+        7: "chunked prefill B=8, 1024 new queries each on a paged P=16 fp8-e4m3 context L_kv~U[2048,16384], "
+           "64q/8kv heads, D=64, step = w=0 call + w=128 call",
     }[cfg]
 
 
@@ -236,6 +243,7 @@ class DecodeBench:
         self.step_bytes = sum(cl["bytes"] for cl in self.calls)
         self.kernels_per_step = sum(2 if cl["S"] > 1 else 1 for cl in self.calls)
         self.unit = "GB/s"
+        self.dtype_name = "bf16" if self.elem == 2 else "fp8-e4m3 kv, bf16 q/out"
         self.e2e_api = "sa_decode with pinned host q/seqlens/page table in, out/lse back; KV cache resident"
 
     def amount(self):
@@ -351,7 +359,8 @@ class PrefillBench:
         self.step_flops = sum(cl["flops"] for cl in self.calls)
         self.kernels_per_step = len(self.calls)
         self.unit = "TFLOP/s"
-        self.elem = 2
+        self.elem = 1 if c.kv.dtype == "e4m3" else 2
+        self.dtype_name = "bf16" if self.elem == 2 else "fp8-e4m3 kv (widened to f16 for the products), bf16 q/out"
         self.e2e_api = "sa_prefill with pinned host q, k, v in, out/lse of both calls back"
         self.B = len(self.q_lens)
         self.maxlen = max(self.kv_lens)
@@ -441,7 +450,7 @@ def run_native(args, world, rank, local):
     torch.cuda.set_device(local)
     dist_init(world, "nccl")
     cfg = args.config
-    wl = PrefillBench(sa, cfg, "cuda") if cfg == 3 else DecodeBench(sa, cfg, "cuda")
+    wl = PrefillBench(sa, cfg, "cuda") if cfg in PREFILL_CONFIGS else DecodeBench(sa, cfg, "cuda")
     stream = torch.cuda.Stream()
     steps = args.steps
     sampler = ClockSampler(local) if rank == 0 else None
@@ -490,7 +499,7 @@ def run_native(args, world, rank, local):
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": wl.unit, "n_gpus": world, "steps": steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 6), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16" if wl.elem == 2 else "fp8-e4m3 kv, bf16 q/out",
+        "vs_baseline": None, "dtype": wl.dtype_name,
         "data": "synthetic (seeded; N(0,1) q/k/v, sinks U(-2,6)); no weights or datasets",
         "config": {"workload": workload_name(cfg), "global_batch": wl.B * world, "seq_len_max": wl.maxlen,
                    "parallelism": "replicas" if world > 1 else "single GPU",
@@ -548,13 +557,13 @@ def run_reference(args, world, rank, local):
         def __getattr__(self, k):
             return getattr(self.inner, k)
 
-    wl = PrefillBench(_Shim(), cfg, dev) if cfg == 3 else DecodeBench(_Shim(), cfg, dev)
+    wl = PrefillBench(_Shim(), cfg, dev) if cfg in PREFILL_CONFIGS else DecodeBench(_Shim(), cfg, dev)
     total_budget = float(args.budget_s)
     steps, warmup = args.steps, args.warmup
     # size the per-step sample from a one-sequence pilot
     dt1, b1, _ = wl.oracle_sample(5.0, max_seqs=1)
     per_step = total_budget / max(1, steps + warmup)
-    n = max(1, min(wl.B if cfg != 3 else 4096, int(per_step / max(dt1, 1e-6))))
+    n = max(1, min(wl.B if cfg not in PREFILL_CONFIGS else 4096, int(per_step / max(dt1, 1e-6))))
     for _ in range(warmup):
         wl.oracle_sample(per_step, max_seqs=n)
     t0 = time.time()
@@ -584,7 +593,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
-    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5, 6, 7])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--budget-s", type=float, default=120.0,
                     help="reference arm: host seconds the whole --steps/--warmup run may take")

@@ -162,8 +162,7 @@ sa_status_t encode_kv_map(CUtensorMap *map, const void *base, bool fp8, const sa
 // ---------------------------------------------------------------- validation
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-sa_status_t check_kv(const sa_kv_desc_t *kv, int32_t batch, int32_t num_qo_heads, int32_t max_kv_len,
-                     bool allow_fp8)
+sa_status_t check_kv(const sa_kv_desc_t *kv, int32_t batch, int32_t num_qo_heads, int32_t max_kv_len)
 {
     if (!kv)
         return fail(SA_ERR_INVALID_ARG, "kv descriptor is NULL");
@@ -171,8 +170,6 @@ sa_status_t check_kv(const sa_kv_desc_t *kv, int32_t batch, int32_t num_qo_heads
         return fail(SA_ERR_INVALID_ARG, "kv->k / kv->v is NULL");
     if (kv->dtype != SA_KV_BF16 && kv->dtype != SA_KV_FP8_E4M3)
         return fail(SA_ERR_INVALID_ARG, "kv->dtype %d is not a sa_kv_dtype_t", (int)kv->dtype);
-    if (kv->dtype == SA_KV_FP8_E4M3 && !allow_fp8)
-        return fail(SA_ERR_UNSUPPORTED, "this call takes a bf16 KV cache only");
     if (kv->num_kv_heads <= 0 || kv->num_pages <= 0 || kv->page_size <= 0 || kv->head_dim <= 0)
         return fail(SA_ERR_INVALID_ARG, "kv sizes must be positive (heads %d, pages %d, page_size %d, dim %d)",
                     kv->num_kv_heads, kv->num_pages, kv->page_size, kv->head_dim);
@@ -269,7 +266,7 @@ sa_status_t check_decode_common(const void *q, const sa_kv_desc_t *kv, const int
         return fail(SA_ERR_UNSUPPORTED, "batch %d > 65535", batch);
     if (!std::isfinite(sm_scale))
         return fail(SA_ERR_INVALID_ARG, "sm_scale must be finite");
-    sa_status_t st = check_kv(kv, batch, num_qo_heads, max_kv_len, true);
+    sa_status_t st = check_kv(kv, batch, num_qo_heads, max_kv_len);
     if (st != SA_OK)
         return st;
     if (batch > 0 && (!q || !seqlens))
@@ -486,7 +483,7 @@ sa_status_t sa_prefill(const void *q, const int32_t *cu_seqlens_q, int32_t total
         return fail(SA_ERR_UNSUPPORTED, "sa_prefill needs sm_scale > 0");
     if (batch > 65535)
         return fail(SA_ERR_UNSUPPORTED, "batch %d > 65535", batch);
-    sa_status_t st = check_kv(kv, batch, num_qo_heads, max_kv_len, false);
+    sa_status_t st = check_kv(kv, batch, num_qo_heads, max_kv_len);
     if (st != SA_OK)
         return st;
     if (batch == 0 || total_q == 0 || max_q_len == 0)
@@ -500,10 +497,11 @@ sa_status_t sa_prefill(const void *q, const int32_t *cu_seqlens_q, int32_t total
     std::memset(&p, 0, sizeof p);
     CUtensorMap tq, tk, tv;
     int dt = 0, dh = 0, dp = 0;
-    st = encode_kv_map(&tk, kv->k, false, kv, 16, &dt, &dh, &dp);
+    const bool fp8 = kv->dtype == SA_KV_FP8_E4M3;
+    st = encode_kv_map(&tk, kv->k, fp8, kv, 16, &dt, &dh, &dp);
     if (st != SA_OK)
         return st;
-    st = encode_kv_map(&tv, kv->v, false, kv, 16, &dt, &dh, &dp);
+    st = encode_kv_map(&tv, kv->v, fp8, kv, 16, &dt, &dh, &dp);
     if (st != SA_OK)
         return st;
     {
@@ -549,10 +547,12 @@ sa_status_t sa_prefill(const void *q, const int32_t *cu_seqlens_q, int32_t total
     p.dim_token = dt;
     p.dim_head = dh;
     p.dim_page = dp;
-    p.score_scale = sm_scale * kLog2e;
+    // FP8: the kernel widens each code to its E4M3 value in f16
+    p.score_scale = sm_scale * kLog2e * (fp8 ? kv->k_scale : 1.f);
+    p.out_scale = fp8 ? kv->v_scale : 1.f;
     if (p.num_q_tiles > 65535)
         return fail(SA_ERR_UNSUPPORTED, "max_q_len too large");
-    e = sa::launch_prefill(tq, tk, tv, p, stream);
+    e = sa::launch_prefill(tq, tk, tv, p, fp8, stream);
     if (e != cudaSuccess)
         return cuda_fail(e, "prefill launch");
     return SA_OK;

@@ -35,6 +35,15 @@
 // round trip) becomes rare.  Causal and window masks (NVIDIA gpt-oss launch
 // article, introduction: full context alternating with a 128-token window)
 // are applied only on tiles that straddle a boundary.
+//
+// FP8-E4M3 caches (vLLM "GPT-OSS optimisations on NVIDIA Blackwell", FP8 KV
+// cache): TMA brings each key tile's E4M3 codes into a 2-slot staging area,
+// and the producer warp widens them (cvt e4m3x2 -> f16x2, exact for every
+// code) into the same f16 tiles (128-byte swizzle) the MMAs read, zeroing
+// rows past the sequence end.  The softmax warps convert their Q tile from
+// bf16 to f16 in place once, P is stored as f16, the products run as
+// kind::f16 with f16 operands, and k_scale (resp. v_scale) is folded into the
+// score scale (resp. the output scale).
 #include <cuda_bf16.h>
 
 #include "sa_internal.h"
@@ -45,26 +54,36 @@ namespace {
 
 constexpr int BM = 128;  // query rows per tile
 constexpr int BN = 64;   // keys per tile
-constexpr int kStages = 4;
 constexpr int kThreads = 320;
 constexpr int kFirstSoftmaxWarp = 2;
 constexpr uint32_t kQTileBytes = BM * kHeadDim * 2;   // 16 KB
 constexpr uint32_t kKVTileBytes = BN * kHeadDim * 2;  // 8 KB
 constexpr uint32_t kBoxBytes = 16 * kHeadDim * 2;     // one 16-key box
+constexpr uint32_t kKV8TileBytes = BN * kHeadDim;     // 4 KB of E4M3 codes
+constexpr uint32_t kBox8Bytes = 16 * kHeadDim;        // one 16-key box of codes
 constexpr uint32_t kTmemCols = 256;
 __host__ __device__ constexpr uint32_t col_s(int t) { return 128u * t; }        // S_t / P_t
 __host__ __device__ constexpr uint32_t col_o(int t) { return 128u * t + 64u; }  // O_t
 constexpr float kLog2e = 1.44269504088896340736f;
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 of the largest tolerated p
-constexpr uint32_t kIdescQK = idesc_bf16_f32(BM, BN, 0);        // Q, K both K-major
-constexpr uint32_t kIdescPV = idesc_bf16_f32(BM, kHeadDim, 1);  // V is MN-major (dims contiguous)
+// Q, K both K-major; V is MN-major (dims contiguous).  f16 operands for an FP8 cache.
+template <bool FP8>
+constexpr uint32_t kIdescQK = idesc_f32acc(BM, BN, 0, FP8);
+template <bool FP8>
+constexpr uint32_t kIdescPV = idesc_f32acc(BM, kHeadDim, 1, FP8);
 
+template <bool FP8>
 struct PrefillSmem {
+    static constexpr int kStages = FP8 ? 3 : 4;  // 16-bit K/V ring (FP8 also stages codes)
     uint8_t q[2][kQTileBytes];
     uint8_t k[kStages][kKVTileBytes];
     uint8_t v[kStages][kKVTileBytes];
+    uint8_t k8[FP8 ? 2 : 1][FP8 ? kKV8TileBytes : 16];  // E4M3 staging (64-byte swizzle)
+    uint8_t v8[FP8 ? 2 : 1][FP8 ? kKV8TileBytes : 16];
     uint64_t q_full;
+    uint64_t q_conv;  // FP8: Q converted to f16
+    uint64_t st_full[2];
     uint64_t k_full[kStages];
     uint64_t v_full[kStages];
     uint64_t kv_empty[kStages];
@@ -73,7 +92,49 @@ struct PrefillSmem {
     uint64_t o_done[2];
     uint32_t tmem_base;
 };
-static_assert(sizeof(PrefillSmem) + 1024 <= 113 * 1024, "two blocks must fit one SM's shared memory");
+static_assert(sizeof(PrefillSmem<false>) + 1024 <= 113 * 1024, "two blocks must fit one SM's shared memory");
+static_assert(sizeof(PrefillSmem<true>) + 1024 <= 113 * 1024, "two blocks must fit one SM's shared memory");
+
+// bf16 pair -> f16 pair (round to nearest; |x| < 65504 assumed).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t x)
+{
+    return pack_f16(__uint_as_float(x << 16), __uint_as_float(x & 0xffff0000u));
+}
+
+// Two E4M3 codes (low byte first) -> their values as f16x2 (exact: every
+// E4M3 value, subnormals included, is an f16 normal).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes)
+{
+    uint32_t d;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"(static_cast<unsigned short>(two_codes)));
+    return d;
+}
+
+// One key tile of E4M3 codes (64 rows of 64 bytes as TMA wrote them with the
+// 64-byte swizzle: 16-byte chunk c of row r at chunk c ^ ((r >> 1) & 3)) ->
+// f16 values in the 128-byte-swizzled layout of a 16-bit tile (chunk c of row
+// r at chunk c ^ (r & 7)).  Rows at or past `valid` become zeros.
+__device__ __forceinline__ void widen_tile(const uint8_t *src, uint8_t *dst, int valid, int lane)
+{
+#pragma unroll 4
+    for (int i = lane; i < BN * 4; i += 32) {
+        const int r = i >> 2, c = i & 3;
+        uint4 w = make_uint4(0u, 0u, 0u, 0u);
+        if (r < valid)
+            w = *reinterpret_cast<const uint4 *>(src + r * 64 + ((c ^ ((r >> 1) & 3)) << 4));
+        uint4 lo, hi;
+        lo.x = e4m3x2_to_f16x2(w.x);
+        lo.y = e4m3x2_to_f16x2(w.x >> 16);
+        lo.z = e4m3x2_to_f16x2(w.y);
+        lo.w = e4m3x2_to_f16x2(w.y >> 16);
+        hi.x = e4m3x2_to_f16x2(w.z);
+        hi.y = e4m3x2_to_f16x2(w.z >> 16);
+        hi.z = e4m3x2_to_f16x2(w.w);
+        hi.w = e4m3x2_to_f16x2(w.w >> 16);
+        *reinterpret_cast<uint4 *>(dst + r * 128 + (((2 * c) ^ (r & 7)) << 4)) = lo;
+        *reinterpret_cast<uint4 *>(dst + r * 128 + (((2 * c + 1) ^ (r & 7)) << 4)) = hi;
+    }
+}
 
 __device__ __forceinline__ void kv_coords(const PrefillParams &p, int slot, int g, int page, int &c1, int &c2,
                                           int &c3)
@@ -110,6 +171,7 @@ __device__ __forceinline__ void mask_tile(uint32_t s_addr, int key0, int pos, in
 // again, forms p = 2^(s*scale - m) (fma.f32x2, ex2; ex2 of -inf is exactly 0),
 // adds p into two paired sums (add.f32x2), packs p to bf16 and stores it as P
 // over the leading columns of S.  When m moved, O is rescaled.
+template <bool FP8>
 __device__ __forceinline__ void softmax_tile(uint32_t s_addr, uint32_t o_addr, float scale, bool o_live, float &m,
                                              float &l)
 {
@@ -151,7 +213,7 @@ __device__ __forceinline__ void softmax_tile(uint32_t s_addr, uint32_t o_addr, f
             const float p0 = ex2(x0);
             const float p1 = ex2(x1);
             ls2[(i >> 1) & 1] = f2_add(ls2[(i >> 1) & 1], f2_pack(p0, p1));
-            pk[i >> 1] = pack_bf16(p0, p1);
+            pk[i >> 1] = FP8 ? pack_f16(p0, p1) : pack_bf16(p0, p1);
         }
         tmem_st8(s_addr + (kChunk / 2) * c, pk);  // P columns [8c, 8c+8): S columns already read
     }
@@ -176,13 +238,15 @@ __device__ __forceinline__ void softmax_tile(uint32_t s_addr, uint32_t o_addr, f
     }
 }
 
+template <bool FP8>
 __global__ void __launch_bounds__(kThreads, 2)
     prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                    const __grid_constant__ CUtensorMap tmv, const PrefillParams p)
 {
+    constexpr int kStages = PrefillSmem<FP8>::kStages;
     extern __shared__ uint8_t smem_raw[];
-    PrefillSmem &sm =
-        *reinterpret_cast<PrefillSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    PrefillSmem<FP8> &sm =
+        *reinterpret_cast<PrefillSmem<FP8> *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int NH = p.heads_per_cta;
@@ -218,6 +282,9 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     if (threadIdx.x == 0) {
         mbar_init(&sm.q_full, 1);
+        mbar_init(&sm.q_conv, 4 * NH);
+        mbar_init(&sm.st_full[0], 1);
+        mbar_init(&sm.st_full[1], 1);
         for (int i = 0; i < kStages; ++i) {
             mbar_init(&sm.k_full[i], 1);
             mbar_init(&sm.v_full[i], 1);
@@ -257,31 +324,76 @@ __global__ void __launch_bounds__(kThreads, 2)
             const int key = (j_first + it) * BN + 16 * lane;
             return trow ? __ldg(trow + key / p.page_size) : b;
         };
-        int next_page = page_of(0);
-        for (int it = 0; it < ntiles; ++it) {
-            const int stage = it % kStages;
-            const int page = next_page;
-            const int nbox = boxes(it);
-            next_page = page_of(it + 1);  // one tile ahead: the table read overlaps the wait
-            if (it >= kStages && !mbar_wait(&sm.kv_empty[stage], ((it / kStages) - 1) & 1, p.status))
-                break;
-            const int key = (j_first + it) * BN + 16 * lane;
-            int c1 = 0, c2 = 0, c3 = 0;
-            if (lane < nbox) {
-                if (page < 0 || page >= p.num_pages)
-                    atomicOr(p.status, SA_DEVICE_BAD_PAGE);  // outside the map: the box reads zeros
-                kv_coords(p, key % p.page_size, g, page, c1, c2, c3);
+        if constexpr (FP8) {
+            // codes of tile it -> staging slot it & 1; the slot's previous
+            // tile was widened (and proxy-fenced) by this warp already
+            auto stage_codes = [&](int it, int page) {
+                const int sb = it & 1;
+                const int nbox = boxes(it);
+                const int key = (j_first + it) * BN + 16 * lane;
+                int c1 = 0, c2 = 0, c3 = 0;
+                if (lane < nbox) {
+                    if (page < 0 || page >= p.num_pages)
+                        atomicOr(p.status, SA_DEVICE_BAD_PAGE);  // outside the map: the box reads zeros
+                    kv_coords(p, key % p.page_size, g, page, c1, c2, c3);
+                }
+                if (lane == 0)
+                    mbar_arrive_expect_tx(&sm.st_full[sb], 2u * static_cast<uint32_t>(nbox) * kBox8Bytes);
+                __syncwarp();
+                if (lane < nbox) {
+                    tma_load_4d(sm.k8[sb] + lane * kBox8Bytes, &tmk, &sm.st_full[sb], 0, c1, c2, c3);
+                    tma_load_4d(sm.v8[sb] + lane * kBox8Bytes, &tmv, &sm.st_full[sb], 0, c1, c2, c3);
+                }
+            };
+            stage_codes(0, page_of(0));
+            int next_page = page_of(1);
+            for (int it = 0; it < ntiles; ++it) {
+                const int stage = it % kStages;
+                if (it + 1 < ntiles) {
+                    stage_codes(it + 1, next_page);
+                    next_page = page_of(it + 2);
+                }
+                if (!mbar_wait(&sm.st_full[it & 1], (it >> 1) & 1, p.status))
+                    break;
+                if (it >= kStages && !mbar_wait(&sm.kv_empty[stage], ((it / kStages) - 1) & 1, p.status))
+                    break;
+                const int valid = min(BN, Lkv - (j_first + it) * BN);
+                widen_tile(sm.k8[it & 1], sm.k[stage], valid, lane);
+                widen_tile(sm.v8[it & 1], sm.v[stage], valid, lane);
+                fence_proxy_async_smem();  // generic writes -> tensor-core reads; staging reads -> next TMA
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&sm.k_full[stage]);
+                    mbar_arrive(&sm.v_full[stage]);
+                }
             }
-            if (lane == 0)
-                mbar_arrive_expect_tx(&sm.k_full[stage], static_cast<uint32_t>(nbox) * kBoxBytes);
-            __syncwarp();
-            if (lane < nbox)
-                tma_load_4d(sm.k[stage] + lane * kBoxBytes, &tmk, &sm.k_full[stage], 0, c1, c2, c3);
-            if (lane == 0)
-                mbar_arrive_expect_tx(&sm.v_full[stage], static_cast<uint32_t>(nbox) * kBoxBytes);
-            __syncwarp();
-            if (lane < nbox)
-                tma_load_4d(sm.v[stage] + lane * kBoxBytes, &tmv, &sm.v_full[stage], 0, c1, c2, c3);
+        } else {
+            int next_page = page_of(0);
+            for (int it = 0; it < ntiles; ++it) {
+                const int stage = it % kStages;
+                const int page = next_page;
+                const int nbox = boxes(it);
+                next_page = page_of(it + 1);  // one tile ahead: the table read overlaps the wait
+                if (it >= kStages && !mbar_wait(&sm.kv_empty[stage], ((it / kStages) - 1) & 1, p.status))
+                    break;
+                const int key = (j_first + it) * BN + 16 * lane;
+                int c1 = 0, c2 = 0, c3 = 0;
+                if (lane < nbox) {
+                    if (page < 0 || page >= p.num_pages)
+                        atomicOr(p.status, SA_DEVICE_BAD_PAGE);  // outside the map: the box reads zeros
+                    kv_coords(p, key % p.page_size, g, page, c1, c2, c3);
+                }
+                if (lane == 0)
+                    mbar_arrive_expect_tx(&sm.k_full[stage], static_cast<uint32_t>(nbox) * kBoxBytes);
+                __syncwarp();
+                if (lane < nbox)
+                    tma_load_4d(sm.k[stage] + lane * kBoxBytes, &tmk, &sm.k_full[stage], 0, c1, c2, c3);
+                if (lane == 0)
+                    mbar_arrive_expect_tx(&sm.v_full[stage], static_cast<uint32_t>(nbox) * kBoxBytes);
+                __syncwarp();
+                if (lane < nbox)
+                    tma_load_4d(sm.v[stage] + lane * kBoxBytes, &tmv, &sm.v_full[stage], 0, c1, c2, c3);
+            }
         }
     } else if (warp == 1) {
         // ============================ MMA issuer ==========================
@@ -295,16 +407,16 @@ __global__ void __launch_bounds__(kThreads, 2)
             const uint64_t dk = dk0 + static_cast<uint64_t>(stage) * (kKVTileBytes >> 4);
 #pragma unroll
             for (int ks = 0; ks < kHeadDim / 16; ++ks)
-                umma_ss(tmem + col_s(t), dq + 2 * ks, dk + 2 * ks, kIdescQK, ks > 0 ? 1u : 0u);
+                umma_ss(tmem + col_s(t), dq + 2 * ks, dk + 2 * ks, kIdescQK<FP8>, ks > 0 ? 1u : 0u);
         };
         auto issue_pv = [&](int t, int stage, bool accumulate) {
             const uint64_t dv = dv0 + static_cast<uint64_t>(stage) * (kKVTileBytes >> 4);
 #pragma unroll
             for (int kk = 0; kk < BN / 16; ++kk)  // K = 16 keys: 8 TMEM columns of P, 2 KB of V
-                umma_ts(tmem + col_o(t), tmem + col_s(t) + 8 * kk, dv + 128 * kk, kIdescPV,
+                umma_ts(tmem + col_o(t), tmem + col_s(t) + 8 * kk, dv + 128 * kk, kIdescPV<FP8>,
                         (accumulate || kk > 0) ? 1u : 0u);
         };
-        bool ok = mbar_wait(&sm.q_full, 0, p.status) && mbar_wait(&sm.k_full[0], 0, p.status);
+        bool ok = mbar_wait(FP8 ? &sm.q_conv : &sm.q_full, 0, p.status) && mbar_wait(&sm.k_full[0], 0, p.status);
         if (ok) {
             tc_fence_after();
             if (lane == 0)
@@ -321,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 break;
             }
             const int key0 = (j_first + it) * BN;
-            if (key0 + BN > Lkv) {
+            if (!FP8 && key0 + BN > Lkv) {  // (the FP8 widening zeroes these rows itself)
                 // value rows past the sequence may hold anything (NaN included):
                 // zero them so that p = 0 contributes exactly 0
                 const int first_bad = max(Lkv - key0, 0);
@@ -378,7 +490,30 @@ __global__ void __launch_bounds__(kThreads, 2)
             l = 1.f;                          // ... and the sum at 1
         }
         bool ok = true;
-        for (int it = 0; it < ntiles; ++it) {
+        if constexpr (FP8) {
+            // this thread's Q row, bf16 -> f16 in place (the swizzle only
+            // permutes 16-byte chunks within the row); lanes start at
+            // different chunks so that no two of 8 lanes share banks
+            ok = mbar_wait(&sm.q_full, 0, p.status);
+            if (ok) {
+                uint4 *qrow = reinterpret_cast<uint4 *>(sm.q[t] + row * 128);
+#pragma unroll
+                for (int c0 = 0; c0 < 8; ++c0) {
+                    const int c = (c0 + lane) & 7;
+                    uint4 w = qrow[c];
+                    w.x = bf16x2_to_f16x2(w.x);
+                    w.y = bf16x2_to_f16x2(w.y);
+                    w.z = bf16x2_to_f16x2(w.z);
+                    w.w = bf16x2_to_f16x2(w.w);
+                    qrow[c] = w;
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&sm.q_conv);
+            }
+        }
+        for (int it = 0; ok && it < ntiles; ++it) {
             if (!mbar_wait(&sm.s_full[t], it & 1, p.status)) {
                 ok = false;
                 break;
@@ -389,7 +524,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 key0 + BN - 1 > p_first || (p.window > 0 && key0 <= p_last - p.window) || key0 + BN > Lkv;
             if (edge)
                 mask_tile(s_addr, key0, pos, Lkv, p.window);
-            softmax_tile(s_addr, o_addr, p.score_scale, it > 0, m, l);
+            softmax_tile<FP8>(s_addr, o_addr, p.score_scale, it > 0, m, l);
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
@@ -399,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         // ---- epilogue: O / l, lse = (m + log2 l) ln 2 ----
         if (ok && mbar_wait(&sm.o_done[t], 0, p.status)) {
             tc_fence_after();
-            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const float inv = l > 0.f ? (FP8 ? p.out_scale : 1.f) / l : 0.f;
             const int64_t orow = static_cast<int64_t>(q_beg + qi) * p.num_qo_heads + h;
             uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.out) + orow * kHeadDim);
 #pragma unroll
@@ -433,35 +568,40 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
 }
 
-size_t prefill_smem_bytes() { return sizeof(PrefillSmem) + 1024; }
+template <bool FP8>
+size_t prefill_smem_bytes()
+{
+    return sizeof(PrefillSmem<FP8>) + 1024;  // + slack for the 1 KB alignment
+}
 
-cudaError_t prepare_prefill()
+template <bool FP8>
+cudaError_t launch_of(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, const PrefillParams &p,
+                      cudaStream_t stream)
 {
     static int done[64] = {0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return e;
-    if (dev >= 0 && dev < 64 && done[dev])
-        return cudaSuccess;
-    e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(prefill_smem_bytes()));
-    if (e == cudaSuccess && dev >= 0 && dev < 64)
-        done[dev] = 1;
-    return e;
+    if (dev < 0 || dev >= 64 || !done[dev]) {
+        e = cudaFuncSetAttribute(prefill_kernel<FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(prefill_smem_bytes<FP8>()));
+        if (e != cudaSuccess)
+            return e;
+        if (dev >= 0 && dev < 64)
+            done[dev] = 1;
+    }
+    const dim3 grid(p.num_qo_heads / p.heads_per_cta, p.num_q_tiles, p.batch);
+    prefill_kernel<FP8><<<grid, kThreads, prefill_smem_bytes<FP8>(), stream>>>(tq, tk, tv, p);
+    return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_prefill(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                           const PrefillParams &p, cudaStream_t stream)
+                           const PrefillParams &p, bool fp8, cudaStream_t stream)
 {
-    cudaError_t e = prepare_prefill();
-    if (e != cudaSuccess)
-        return e;
-    const dim3 grid(p.num_qo_heads / p.heads_per_cta, p.num_q_tiles, p.batch);
-    prefill_kernel<<<grid, kThreads, prefill_smem_bytes(), stream>>>(tq, tk, tv, p);
-    return cudaGetLastError();
+    return fp8 ? launch_of<true>(tq, tk, tv, p, stream) : launch_of<false>(tq, tk, tv, p, stream);
 }
 
 }  // namespace sa

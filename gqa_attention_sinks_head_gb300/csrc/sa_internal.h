@@ -56,7 +56,8 @@ struct PrefillParams {
     int32_t page_size, table_stride, num_pages, max_q_len, max_kv_len;
     int32_t window, num_q_tiles;
     int32_t dim_token, dim_head, dim_page;  // tensor-map dimension (1..3) of each KV coordinate
-    float score_scale;                      // sm_scale * log2(e)
+    float score_scale;                      // sm_scale * log2(e) (* k_scale for an FP8 cache)
+    float out_scale;                        // 1 (v_scale for an FP8 cache)
 };
 
 // Record `fmt` as the calling thread's sa_last_error() message and return st.
@@ -68,6 +69,6 @@ cudaError_t launch_decode(const CUtensorMap &tk, const CUtensorMap &tv, const De
 cudaError_t decode_occupancy(bool fp8, int *blocks_per_sm);
 cudaError_t launch_merge(const MergeParams &p, cudaStream_t stream);
 cudaError_t launch_prefill(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                           const PrefillParams &p, cudaStream_t stream);
+                           const PrefillParams &p, bool fp8, cudaStream_t stream);
 
 }  // namespace sa

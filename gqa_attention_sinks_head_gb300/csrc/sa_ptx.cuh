@@ -428,11 +428,11 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
 
 // Instruction descriptor, kind::f16: f32 accumulator, bf16 A and B, A K-major,
 // B K-major (b_mn_major = 0) or MN-major (1), M x N.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int b_mn_major)
+__host__ __device__ constexpr uint32_t idesc_f32acc(int M, int N, int b_mn_major, bool f16 = false)
 {
     return (1u << 4)                                   // D format: f32
-           | (1u << 7)                                 // A format: bf16
-           | (1u << 10)                                // B format: bf16
+           | ((f16 ? 0u : 1u) << 7)                    // A format: f16 (0) or bf16 (1)
+           | ((f16 ? 0u : 1u) << 10)                   // B format: same as A
            | (static_cast<uint32_t>(b_mn_major) << 16) // B major
            | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
            | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16

@@ -214,8 +214,10 @@ sa_status_t sa_merge_states(const float *o_part, const float *lse_part, int32_t 
  *   cu_seqlens_q device int32 [batch + 1], cu[0] = 0, non-decreasing
  *   total_q      rows of q and out (= cu_seqlens_q[batch]); the kernels read and
  *                write no row at or past it
- *   kv           KV cache descriptor (bf16 only); holds each sequence's keys,
- *                the queries' own keys included
+ *   kv           KV cache descriptor, bf16 or FP8-E4M3; holds each sequence's
+ *                keys, the queries' own keys included.  With an FP8 cache the
+ *                products run in f16: q is rounded to f16 (|q| < 65504 assumed)
+ *                and the codes are widened exactly
  *   seqlens_kv   device int32 [batch]: keys of sequence b (L_kv,b >= L_q,b)
  *   max_q_len, max_kv_len  host upper bounds on the query / key lengths
  *   sinks, window as sa_decode; sm_scale > 0 (SA_ERR_UNSUPPORTED otherwise)

@@ -54,3 +54,34 @@ def test_config5_decode_fp8_b256(sa, oracle, window):
     else:
         seqs = sorted(np.random.default_rng(55).choice(256, 6, replace=False).tolist())
     _sampled(oracle, case, out, lse, seqs, "config 5 w=%d" % window)
+
+
+@pytest.mark.parametrize("window", [0, 128])
+def test_config6_chunked_paged_prefill(sa, oracle, window):
+    """Chunked prefill: 1024 new queries per sequence on paged contexts of
+    2k-16k keys, bottom-right causal.  Every output of a seeded sample of rows
+    (each sequence's first and last row and each 128-row tile's edges)."""
+    from sa_testlib import oracle_prefill, prefill_gpu
+    case = W.make_config(6, window=window)
+    out, lse = prefill_gpu(sa, case.to("cuda"))
+    assert sa.sa_device_status() == 0
+    g = np.random.default_rng(66)
+    edges = np.concatenate([np.arange(0, 8192, 128), np.arange(127, 8192, 128)])
+    sel = np.unique(np.concatenate([edges[g.choice(len(edges), 48, replace=False)],
+                                    np.arange(0, 8192, 1024), np.arange(1023, 8192, 1024),
+                                    g.choice(8192, 32, replace=False)])).astype(np.int32)
+    ref_o, ref_l = oracle_prefill(oracle, case, sel)
+    check_close(out[sel], lse[sel], ref_o, ref_l, "config 6 w=%d" % window)
+
+
+def test_config7_chunked_paged_prefill_fp8(sa, oracle):
+    """Workload 6 on an FP8-E4M3 cache, window 0, sampled rows."""
+    from sa_testlib import oracle_prefill, prefill_gpu
+    case = W.make_config(7, window=0)
+    out, lse = prefill_gpu(sa, case.to("cuda"))
+    assert sa.sa_device_status() == 0
+    g = np.random.default_rng(77)
+    sel = np.unique(np.concatenate([np.arange(0, 8192, 1024), np.arange(1023, 8192, 1024),
+                                    g.choice(8192, 48, replace=False)])).astype(np.int32)
+    ref_o, ref_l = oracle_prefill(oracle, case, sel)
+    check_close(out[sel], lse[sel], ref_o, ref_l, "config 7")

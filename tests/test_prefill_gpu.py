@@ -77,3 +77,31 @@ def test_config3_full_size_sampled_rows(sa, oracle, window):
     sel = np.unique(np.concatenate([np.arange(0, 8192, 128), np.arange(127, 8192, 128),
                                     g.choice(8192, 128, replace=False)])).astype(np.int32)
     run(sa, oracle, case, "config 3 w=%d" % window, sel=sel)
+
+
+# ---- FP8-E4M3 cache: codes widened exactly, products in f16 ---------------
+@pytest.mark.parametrize("T", [1, 63, 129, 700])
+@pytest.mark.parametrize("window", [0, 128])
+def test_fp8_single_sequence(sa, oracle, T, window):
+    case = W.make_prefill_case([T], [T], window=window, kv_dtype="e4m3", seed=300 + T)
+    run(sa, oracle, case, "fp8 T=%d w=%d" % (T, window))
+
+
+@pytest.mark.parametrize("layout", ["HND", "NHD"])
+@pytest.mark.parametrize("window", [0, 128])
+def test_fp8_paged_ragged(sa, oracle, layout, window):
+    # chunked prefill on a paged FP8 cache: L_q < L_kv, sequence ends inside tiles
+    case = W.make_prefill_case([200, 77, 5, 130], [520, 77, 1000, 131], paged=True, page_size=16, layout=layout,
+                               window=window, kv_dtype="e4m3", poison_pages=5, seed=310)
+    run(sa, oracle, case, "fp8 paged %s w=%d" % (layout, window))
+
+
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (6, 2)])
+def test_fp8_group_pairings(sa, oracle, hq, hkv):
+    case = W.make_prefill_case([150], [150], num_qo_heads=hq, num_kv_heads=hkv, kv_dtype="e4m3", seed=311)
+    run(sa, oracle, case, "fp8 Hq=%d Hkv=%d" % (hq, hkv))
+
+
+def test_fp8_peaked_scores_no_sinks(sa, oracle):
+    case = W.make_prefill_case([300], [300], sm_scale=1.5, sinks=False, kv_dtype="e4m3", seed=312)
+    run(sa, oracle, case, "fp8 scale 1.5, no sink")

@@ -221,7 +221,7 @@ def make_decode_case(seqlens, *, num_qo_heads=64, num_kv_heads=8, head_dim=64, p
 
 def make_prefill_case(q_lens, kv_lens, *, num_qo_heads=64, num_kv_heads=8, head_dim=64,
                       page_size=None, paged=False, window=0, sm_scale=0.125, sinks=True,
-                      poison_pages=0, seed=0, device="cpu", layout="NHD", name="") -> Case:
+                      poison_pages=0, seed=0, device="cpu", layout="NHD", kv_dtype="bf16", name="") -> Case:
     """Ragged prefill: sequence b has q_lens[b] queries (the last ones of its
     kv_lens[b] keys).  Contiguous NHD K/V by default: one page per sequence."""
     ql = [int(x) for x in q_lens]
@@ -231,7 +231,7 @@ def make_prefill_case(q_lens, kv_lens, *, num_qo_heads=64, num_kv_heads=8, head_
         page_size = max(kl + [1]) if not paged else 16
         if not paged:
             page_size = ((page_size + 127) // 128) * 128
-    kv = make_kv(kl, num_kv_heads, head_dim, page_size, paged=paged, kv_dtype="bf16",
+    kv = make_kv(kl, num_kv_heads, head_dim, page_size, paged=paged, kv_dtype=kv_dtype,
                  poison_pages=poison_pages, seed=seed + 11, device=device, layout=layout)
     g = _gen(seed + 3, device)
     T = sum(ql)
@@ -259,6 +259,9 @@ def config_seqlens(cfg: int):
         return [32768] * 128
     if cfg == 5:
         return [8192] * 256
+    if cfg == 6:
+        g = _gen(CONFIG_SEED + 6, "cpu")
+        return torch.randint(2048, 16384 + 1, (8,), generator=g).tolist()
     raise ValueError(cfg)
 
 
@@ -271,6 +274,10 @@ def make_config(cfg: int, *, window: int = 0, device="cpu") -> Case:
     3: prefill, one 8192-token sequence, contiguous bf16 NHD; window 0 or 128.
     4: decode, B=128, L=32768, paged bf16 (262,144 pages), split-KV.
     5: decode, B=256, L=8192, paged FP8-E4M3 (per-tensor scales); window 0 or 128.
+    6: chunked prefill, B=8: each sequence appends 1024 queries to its paged
+       context, L_kv ~ U[2048, 16384] (P=16, permuted table, HND, 64 poison
+       pages), bottom-right causal; window 0 or 128.
+    7: workload 6 on an FP8-E4M3 cache (per-tensor scales).
     """
     seed = CONFIG_SEED + cfg
     if cfg == 1:
@@ -291,6 +298,13 @@ def make_config(cfg: int, *, window: int = 0, device="cpu") -> Case:
         return make_decode_case(config_seqlens(5), page_size=16, paged=True, kv_dtype="e4m3",
                                 window=window, seed=seed, device=device,
                                 name="decode B=256 L=8192 paged P=16 fp8-e4m3 w=%d" % window)
+    if cfg in (6, 7):
+        kl = config_seqlens(6)
+        dt = "bf16" if cfg == 6 else "e4m3"
+        return make_prefill_case([1024] * len(kl), kl, paged=True, page_size=16, layout="HND", window=window,
+                                 poison_pages=64, seed=seed, device=device, kv_dtype=dt,
+                                 name="chunked prefill B=8 Lq=1024 L_kv~U[2048,16384] paged P=16 %s w=%d"
+                                 % (dt, window))
     raise ValueError(cfg)
 
 
