@@ -75,15 +75,16 @@ constexpr uint32_t kIdescPV = idesc_f32acc(BM, kHeadDim, 1, FP8);
 
 template <bool FP8>
 struct PrefillSmem {
-    static constexpr int kStages = FP8 ? 3 : 4;  // 16-bit K/V ring (FP8 also stages codes)
+    static constexpr int kStages = FP8 ? 2 : 4;  // 16-bit K/V ring
+    static constexpr int kStaged = FP8 ? 4 : 1;  // FP8: slots of E4M3 codes in flight
     uint8_t q[2][kQTileBytes];
     uint8_t k[kStages][kKVTileBytes];
     uint8_t v[kStages][kKVTileBytes];
-    uint8_t k8[FP8 ? 2 : 1][FP8 ? kKV8TileBytes : 16];  // E4M3 staging (64-byte swizzle)
-    uint8_t v8[FP8 ? 2 : 1][FP8 ? kKV8TileBytes : 16];
+    uint8_t k8[kStaged][FP8 ? kKV8TileBytes : 16];  // E4M3 staging (64-byte swizzle)
+    uint8_t v8[kStaged][FP8 ? kKV8TileBytes : 16];
     uint64_t q_full;
     uint64_t q_conv;  // FP8: Q converted to f16
-    uint64_t st_full[2];
+    uint64_t st_full[kStaged];
     uint64_t k_full[kStages];
     uint64_t v_full[kStages];
     uint64_t kv_empty[kStages];
@@ -283,8 +284,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (threadIdx.x == 0) {
         mbar_init(&sm.q_full, 1);
         mbar_init(&sm.q_conv, 4 * NH);
-        mbar_init(&sm.st_full[0], 1);
-        mbar_init(&sm.st_full[1], 1);
+        for (int i = 0; i < PrefillSmem<FP8>::kStaged; ++i)
+            mbar_init(&sm.st_full[i], 1);
         for (int i = 0; i < kStages; ++i) {
             mbar_init(&sm.k_full[i], 1);
             mbar_init(&sm.v_full[i], 1);
@@ -325,12 +326,15 @@ __global__ void __launch_bounds__(kThreads, 2)
             return trow ? __ldg(trow + key / p.page_size) : b;
         };
         if constexpr (FP8) {
-            // codes of tile it -> staging slot it & 1; the slot's previous
-            // tile was widened (and proxy-fenced) by this warp already
-            auto stage_codes = [&](int it, int page) {
-                const int sb = it & 1;
-                const int nbox = boxes(it);
-                const int key = (j_first + it) * BN + 16 * lane;
+            // codes of tile j -> staging slot j % kStaged, up to kStaged tiles
+            // ahead; a slot is reused only after this warp widened (and
+            // proxy-fenced) the tile it held
+            constexpr int kStaged = PrefillSmem<FP8>::kStaged;
+            auto stage_codes = [&](int j) {
+                const int sb = j % kStaged;
+                const int nbox = boxes(j);
+                const int page = page_of(j);
+                const int key = (j_first + j) * BN + 16 * lane;
                 int c1 = 0, c2 = 0, c3 = 0;
                 if (lane < nbox) {
                     if (page < 0 || page >= p.num_pages)
@@ -345,21 +349,19 @@ __global__ void __launch_bounds__(kThreads, 2)
                     tma_load_4d(sm.v8[sb] + lane * kBox8Bytes, &tmv, &sm.st_full[sb], 0, c1, c2, c3);
                 }
             };
-            stage_codes(0, page_of(0));
-            int next_page = page_of(1);
+            int issued = 0;
             for (int it = 0; it < ntiles; ++it) {
                 const int stage = it % kStages;
-                if (it + 1 < ntiles) {
-                    stage_codes(it + 1, next_page);
-                    next_page = page_of(it + 2);
-                }
-                if (!mbar_wait(&sm.st_full[it & 1], (it >> 1) & 1, p.status))
+                for (; issued < ntiles && issued < it + kStaged; ++issued)
+                    stage_codes(issued);
+                const int sb = it % kStaged;
+                if (!mbar_wait(&sm.st_full[sb], (it / kStaged) & 1, p.status))
                     break;
                 if (it >= kStages && !mbar_wait(&sm.kv_empty[stage], ((it / kStages) - 1) & 1, p.status))
                     break;
                 const int valid = min(BN, Lkv - (j_first + it) * BN);
-                widen_tile(sm.k8[it & 1], sm.k[stage], valid, lane);
-                widen_tile(sm.v8[it & 1], sm.v[stage], valid, lane);
+                widen_tile(sm.k8[sb], sm.k[stage], valid, lane);
+                widen_tile(sm.v8[sb], sm.v[stage], valid, lane);
                 fence_proxy_async_smem();  // generic writes -> tensor-core reads; staging reads -> next TMA
                 __syncwarp();
                 if (lane == 0) {
