@@ -34,7 +34,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "sink-attn decode HBM GB/s (% peak); prefill TFLOP/s (% bf16 tensor peak)"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-DEFAULT_STEPS = {1: 2000, 2: 2000, 3: 50, 4: 100, 5: 500, 6: 50, 7: 50}
+DEFAULT_STEPS = {1: 2000, 2: 2000, 3: 50, 4: 100, 5: 500, 6: 50, 7: 50, 8: 1000}
 
 
 # ------------------------------------------------------------------ helpers
@@ -180,6 +180,14 @@ def decode_bytes(seqlens, window, hkv, hq, dim, elem_bytes, with_lse=True):
     return keys * hkv * dim * 2 * elem_bytes + 2 * b * hq * dim * 2 + (4 * b * hq if with_lse else 0)
 
 
+def multi_bytes(seqlens, window, q_len, hkv, hq, dim, elem_bytes):
+    """Algorithmic HBM bytes of one multi-token decode call: every key visible
+    to any of a sequence's q_len tokens once per kv head, plus q, out, lse."""
+    keys = sum(min(int(L), window + q_len - 1) if window > 0 else int(L) for L in seqlens)
+    rows = len(seqlens) * q_len
+    return keys * hkv * dim * 2 * elem_bytes + 2 * rows * hq * dim * 2 + 4 * rows * hq
+
+
 def prefill_flops(q_lens, kv_lens, window, hq, dim):
     """4 * Hq * D * sum over queries of the visible keys (QK and PV)."""
     tot = 0
@@ -192,10 +200,11 @@ def prefill_flops(q_lens, kv_lens, window, hq, dim):
 
 
 def windows_of(cfg):
-    return {1: [0], 2: [0, 128], 3: [0, 128], 4: [0], 5: [0, 128, 0, 128], 6: [0, 128], 7: [0, 128]}[cfg]
+    return {1: [0], 2: [0, 128], 3: [0, 128], 4: [0], 5: [0, 128, 0, 128], 6: [0, 128], 7: [0, 128], 8: [0, 128]}[cfg]
 
 
 PREFILL_CONFIGS = (3, 6, 7)
+MULTI_CONFIGS = (8,)
 
 
 def workload_name(cfg):
@@ -209,6 +218,8 @@ def workload_name(cfg):
            "64q/8kv heads, D=64, step = w=0 call + w=128 call",
         7: "chunked prefill B=8, 1024 new queries each on a paged P=16 fp8-e4m3 context L_kv~U[2048,16384], "
            "64q/8kv heads, D=64, step = w=0 call + w=128 call",
+        8: "multi-token decode B=64, 4 new tokens each, L~U[1024,8192] paged P=16 bf16, 64q/8kv heads, D=64, "
+           "step = w=0 call + w=128 call",
     }[cfg]
 
 
@@ -336,6 +347,124 @@ class DecodeBench:
         return dt, nbytes, desc
 
 
+class MultiDecodeBench:
+    """One step = the multi-token decode calls of the workload (w=0, w=128) on
+    one resident cache; each call is one sa_decode_multi (decode kernel, plus
+    the merge kernel when split), timed as a whole."""
+
+    def __init__(self, sa, cfg, device):
+        import torch
+        import workloads as W
+        self.sa, self.cfg, self.torch = sa, cfg, torch
+        self.case = W.make_config(cfg, window=0, device=device)
+        c = self.case
+        self.R, self.Hq, self.D = c.q.shape
+        self.Hkv = c.kv.num_kv_heads
+        self.seqlens = [int(x) for x in c.seqlens.cpu()]
+        self.B = len(self.seqlens)
+        self.q_len = self.R // self.B
+        self.maxlen = max(self.seqlens)
+        self.elem = 1 if c.kv.dtype == "e4m3" else 2
+        self.calls = []
+        for w in windows_of(cfg):
+            S = sa.sa_decode_num_splits(self.B, self.Hkv, self.maxlen, w)
+            nbytes = sa.sa_decode_multi_workspace_size(self.B, self.q_len, self.Hq, self.Hkv, self.D, self.maxlen,
+                                                       w, S)
+            self.calls.append(dict(
+                window=w, S=S, ws=torch.empty(max(nbytes, 16), dtype=torch.uint8, device=device),
+                out=torch.empty(self.R, self.Hq, self.D, dtype=torch.bfloat16, device=device),
+                lse=torch.empty(self.R, self.Hq, dtype=torch.float32, device=device),
+                bytes=multi_bytes(self.seqlens, w, self.q_len, self.Hkv, self.Hq, self.D, self.elem)))
+        self.step_bytes = sum(cl["bytes"] for cl in self.calls)
+        self.kernels_per_step = sum(2 if cl["S"] > 1 else 1 for cl in self.calls)
+        self.unit = "GB/s"
+        self.dtype_name = "bf16" if self.elem == 2 else "fp8-e4m3 kv, bf16 q/out"
+        self.e2e_api = ("sa_decode_multi with pinned host q/seqlens/page table in, out/lse back; "
+                        "KV cache resident")
+
+    def amount(self):
+        return self.step_bytes / 1e9
+
+    def run_call(self, cl, stream, ev=None):
+        c = self.case
+        if ev is not None:
+            ev[0].record(stream)
+        self.sa.sa_decode_multi(c.q, self.q_len, c.kv, c.seqlens, c.sinks, cl["window"], c.sm_scale, cl["out"],
+                                cl["lse"], max_kv_len=self.maxlen, workspace=cl["ws"], num_splits=cl["S"],
+                                stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+
+    def step(self, stream, evs=None):
+        for i, cl in enumerate(self.calls):
+            self.run_call(cl, stream, None if evs is None else evs[i])
+
+    def dominant(self):
+        return 0, "decode_kernel (with its merge)", self.calls[0]["bytes"]
+
+    def e2e(self, stream, steps, warmup):
+        torch = self.torch
+        c = self.case
+        hq = torch.empty(c.q.shape, dtype=c.q.dtype, pin_memory=True).copy_(c.q.cpu())
+        hs = torch.empty(c.seqlens.shape, dtype=torch.int32, pin_memory=True).copy_(c.seqlens.cpu())
+        ht = torch.empty(c.kv.page_table.shape, dtype=torch.int32, pin_memory=True).copy_(c.kv.page_table.cpu())
+        houts = [(torch.empty(cl["out"].shape, dtype=torch.bfloat16, pin_memory=True),
+                  torch.empty(cl["lse"].shape, dtype=torch.float32, pin_memory=True)) for cl in self.calls]
+        h2d = hq.numel() * 2 + hs.numel() * 4 + ht.numel() * 4
+        d2h = sum(o.numel() * 2 + l.numel() * 4 for o, l in houts)
+
+        def one():
+            c.q.copy_(hq, non_blocking=True)
+            c.seqlens.copy_(hs, non_blocking=True)
+            c.kv.page_table.copy_(ht, non_blocking=True)
+            for cl, (ho, hl) in zip(self.calls, houts):
+                self.run_call(cl, stream)
+                ho.copy_(cl["out"], non_blocking=True)
+                hl.copy_(cl["lse"], non_blocking=True)
+
+        with torch.cuda.stream(stream):
+            for _ in range(warmup):
+                one()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(steps):
+                one()
+            e1.record(stream)
+            torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps, h2d, d2h
+
+    def oracle_sample(self, budget_s, max_seqs=None):
+        """Every token row of the first n sequences, all heads, every call."""
+        import numpy as np
+        import oracle
+        oracle.build()
+        c = self.case
+        cpu = c.to("cpu")
+        n = self.B if max_seqs is None else max(1, min(self.B, max_seqs))
+        rows = oracle.prefill_rows(cpu.cu_seqlens_q, cpu.seqlens)
+        sel = np.arange(n * self.q_len, dtype=np.int32)
+        sr = np.repeat(sel, self.Hq)
+        sh = np.tile(np.arange(self.Hq, dtype=np.int32), len(sel))
+        t0 = time.time()
+        nbytes = 0
+        for cl in self.calls:
+            oracle.attend(cpu.q, rows[0], rows[1], cpu.kv.as_dict(), cpu.seqlens, cpu.sinks, cl["window"],
+                          cpu.sm_scale, sr, sh)
+            nbytes += multi_bytes(self.seqlens[:n], cl["window"], self.q_len, self.Hkv, self.Hq, self.D, self.elem)
+        dt = time.time() - t0
+        return dt, nbytes, "%d of %d sequences x %d tokens x %d heads, every call of the step" % (
+            n, self.B, self.q_len, self.Hq)
+
+
+def make_bench(sa, cfg, device):
+    if cfg in PREFILL_CONFIGS:
+        return PrefillBench(sa, cfg, device)
+    if cfg in MULTI_CONFIGS:
+        return MultiDecodeBench(sa, cfg, device)
+    return DecodeBench(sa, cfg, device)
+
+
 class PrefillBench:
     """One step = the prefill calls of the workload (full context, then window 128)."""
 
@@ -450,7 +579,7 @@ def run_native(args, world, rank, local):
     torch.cuda.set_device(local)
     dist_init(world, "nccl")
     cfg = args.config
-    wl = PrefillBench(sa, cfg, "cuda") if cfg in PREFILL_CONFIGS else DecodeBench(sa, cfg, "cuda")
+    wl = make_bench(sa, cfg, "cuda")
     stream = torch.cuda.Stream()
     steps = args.steps
     sampler = ClockSampler(local) if rank == 0 else None
@@ -557,7 +686,7 @@ def run_reference(args, world, rank, local):
         def __getattr__(self, k):
             return getattr(self.inner, k)
 
-    wl = PrefillBench(_Shim(), cfg, dev) if cfg in PREFILL_CONFIGS else DecodeBench(_Shim(), cfg, dev)
+    wl = make_bench(_Shim(), cfg, dev)
     total_budget = float(args.budget_s)
     steps, warmup = args.steps, args.warmup
     # size the per-step sample from a one-sequence pilot
@@ -593,7 +722,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
-    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5, 6, 7])
+    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5, 6, 7, 8])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--budget-s", type=float, default=120.0,
                     help="reference arm: host seconds the whole --steps/--warmup run may take")

@@ -16,6 +16,7 @@ import os
 __all__ = [
     "SinkAttnError", "KVDesc", "load", "build", "sa_decode", "sa_decode_partial", "sa_merge_states",
     "sa_prefill", "sa_decode_static_workspace", "sa_decode_num_splits", "sa_decode_workspace_size", "sa_device_status", "sa_version",
+    "sa_decode_multi", "sa_decode_multi_workspace_size", "SA_MAX_DECODE_TOKENS",
     "SA_KV_BF16", "SA_KV_FP8_E4M3", "kv_desc",
 ]
 
@@ -28,7 +29,8 @@ SA_DEVICE_SEQLEN_RANGE, SA_DEVICE_BAD_PAGE, SA_DEVICE_TIMEOUT, SA_DEVICE_BAD_QLE
 
 EXPORTS = ["sa_decode", "sa_decode_num_splits", "sa_decode_workspace_size", "sa_decode_partial",
            "sa_merge_states", "sa_prefill", "sa_device_status", "sa_status_string", "sa_last_error",
-           "sa_version", "sa_decode_static_workspace"]
+           "sa_version", "sa_decode_static_workspace", "sa_decode_multi", "sa_decode_multi_workspace_size"]
+SA_MAX_DECODE_TOKENS = 8
 SA_STATIC_WORKSPACE_BYTES = 16 << 20
 
 
@@ -74,6 +76,9 @@ def load(path: str | None = None):
     KP = ctypes.POINTER(KVDesc)
     lib.sa_decode.argtypes = [P, KP, P, i32, i32, i32, P, i32, f32, P, P, P, sz, i32, P]
     lib.sa_decode_static_workspace.argtypes = [P, KP, P, i32, i32, i32, P, i32, f32, P, P, i32, P]
+    lib.sa_decode_multi.argtypes = [P, i32, KP, P, i32, i32, i32, P, i32, f32, P, P, P, sz, i32, P]
+    lib.sa_decode_multi_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32]
+    lib.sa_decode_multi_workspace_size.restype = sz
     lib.sa_decode_partial.argtypes = [P, KP, P, i32, i32, i32, i32, f32, i32, P, P, P]
     lib.sa_merge_states.argtypes = [P, P, i32, i32, i32, i32, P, P, P, P]
     lib.sa_prefill.argtypes = [P, P, i32, KP, P, i32, i32, i32, i32, P, i32, f32, P, P, P]
@@ -86,7 +91,8 @@ def load(path: str | None = None):
     lib.sa_status_string.restype = ctypes.c_char_p
     lib.sa_last_error.restype = ctypes.c_char_p
     lib.sa_version.restype = ctypes.c_int
-    for fn in ("sa_decode", "sa_decode_static_workspace", "sa_decode_partial", "sa_merge_states", "sa_prefill", "sa_device_status"):
+    for fn in ("sa_decode", "sa_decode_static_workspace", "sa_decode_partial", "sa_merge_states", "sa_prefill",
+               "sa_device_status", "sa_decode_multi"):
         getattr(lib, fn).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -154,6 +160,29 @@ def sa_decode(q, kv, seqlens, sinks, window, sm_scale, out, lse=None, *, max_kv_
                          int(window), float(sm_scale), _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes,
                          int(num_splits), _stream(stream)))
     return out, lse
+
+
+def sa_decode_multi(q, q_len, kv, seqlens, sinks, window, sm_scale, out, lse=None, *, max_kv_len, workspace=None,
+                    num_splits=0, stream=None):
+    """sa_decode_multi on torch CUDA tensors: q, out [batch * q_len, Hq, 64],
+    token k of sequence b in row b * q_len + k; writes `out` (and `lse`)."""
+    lib = load()
+    desc, keep = kv_desc(kv)
+    R, Hq, _ = q.shape
+    B = seqlens.shape[0]
+    if R != B * int(q_len):
+        raise ValueError("q has %d rows, expected batch * q_len = %d" % (R, B * int(q_len)))
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.sa_decode_multi(_ptr(q), int(q_len), ctypes.byref(desc), _ptr(seqlens), B, Hq, int(max_kv_len),
+                               _ptr(sinks), int(window), float(sm_scale), _ptr(out), _ptr(lse), _ptr(workspace),
+                               ws_bytes, int(num_splits), _stream(stream)))
+    return out, lse
+
+
+def sa_decode_multi_workspace_size(batch, q_len, num_qo_heads, num_kv_heads, head_dim, max_kv_len, window,
+                                   num_splits=0):
+    return int(load().sa_decode_multi_workspace_size(int(batch), int(q_len), int(num_qo_heads), int(num_kv_heads),
+                                                     int(head_dim), int(max_kv_len), int(window), int(num_splits)))
 
 
 def sa_decode_static_workspace(q, kv, seqlens, sinks, window, sm_scale, out, lse=None, *, max_kv_len,

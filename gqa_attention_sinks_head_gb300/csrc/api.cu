@@ -213,12 +213,12 @@ sa_status_t check_kv(const sa_kv_desc_t *kv, int32_t batch, int32_t num_qo_heads
     return SA_OK;
 }
 
-int32_t eff_tiles(int32_t max_kv_len, int32_t window)
+int32_t eff_tiles(int32_t max_kv_len, int32_t window, int32_t q_len = 1)
 {
     if (max_kv_len <= 0)
         return 0;
-    if (window > 0)
-        return (std::min(window, max_kv_len) + 15 + sa::kTile - 1) / sa::kTile;
+    if (window > 0)  // the q_len tokens' windows span window + q_len - 1 keys, not tile-aligned
+        return (std::min(window + q_len - 1, max_kv_len) + 15 + sa::kTile - 1) / sa::kTile;
     return (max_kv_len + sa::kTile - 1) / sa::kTile;
 }
 
@@ -276,10 +276,10 @@ sa_status_t check_decode_common(const void *q, const sa_kv_desc_t *kv, const int
     return SA_OK;
 }
 
-sa_status_t launch_decode_kernel(const void *q, const sa_kv_desc_t *kv, const int32_t *seqlens, int32_t batch,
-                                 int32_t num_qo_heads, int32_t max_kv_len, const float *sinks, int32_t window,
-                                 float sm_scale, void *out, float *lse, float *o_part, float *lse_part,
-                                 int32_t S, bool partial, cudaStream_t stream)
+sa_status_t launch_decode_kernel(const void *q, int32_t q_len, const sa_kv_desc_t *kv, const int32_t *seqlens,
+                                 int32_t batch, int32_t num_qo_heads, int32_t max_kv_len, const float *sinks,
+                                 int32_t window, float sm_scale, void *out, float *lse, float *o_part,
+                                 float *lse_part, int32_t S, bool partial, cudaStream_t stream)
 {
     const bool fp8 = kv->dtype == SA_KV_FP8_E4M3;
     sa::DecodeParams p;
@@ -310,13 +310,14 @@ sa_status_t launch_decode_kernel(const void *q, const sa_kv_desc_t *kv, const in
     p.num_qo_heads = num_qo_heads;
     p.num_kv_heads = kv->num_kv_heads;
     p.group = num_qo_heads / kv->num_kv_heads;
+    p.q_len = q_len;
     p.page_size = kv->page_size;
     p.table_stride = kv->page_table_stride;
     p.num_pages = kv->num_pages;
     p.max_kv_len = max_kv_len;
     p.window = window;
     p.num_splits = S;
-    p.tiles_per_split = std::max<int32_t>(1, (eff_tiles(max_kv_len, window) + S - 1) / S);
+    p.tiles_per_split = std::max<int32_t>(1, (eff_tiles(max_kv_len, window, q_len) + S - 1) / S);
     p.partial = partial ? 1 : 0;
     p.dim_token = dt;
     p.dim_head = dh;
@@ -378,29 +379,39 @@ size_t sa_decode_workspace_size(int32_t batch, int32_t num_qo_heads, int32_t num
     return S <= 1 ? 0 : partial_bytes(S, batch, num_qo_heads, head_dim);
 }
 
-sa_status_t sa_decode(const void *q, const sa_kv_desc_t *kv, const int32_t *seqlens, int32_t batch,
-                      int32_t num_qo_heads, int32_t max_kv_len, const float *sinks, int32_t window,
-                      float sm_scale, void *out, float *lse, void *workspace, size_t workspace_bytes,
-                      int32_t num_splits, cudaStream_t stream)
+}  // extern "C"
+
+namespace {
+
+// sa_decode and sa_decode_multi: rows = batch * q_len query rows.
+sa_status_t decode_impl(const void *q, int32_t q_len, const sa_kv_desc_t *kv, const int32_t *seqlens,
+                        int32_t batch, int32_t num_qo_heads, int32_t max_kv_len, const float *sinks,
+                        int32_t window, float sm_scale, void *out, float *lse, void *workspace,
+                        size_t workspace_bytes, int32_t num_splits, cudaStream_t stream)
 {
     g_err[0] = 0;
     sa_status_t st = check_decode_common(q, kv, seqlens, batch, num_qo_heads, max_kv_len, window, sm_scale);
     if (st != SA_OK)
         return st;
+    if (q_len < 1 || q_len > SA_MAX_DECODE_TOKENS)
+        return fail(SA_ERR_UNSUPPORTED, "q_len %d outside [1, %d]", q_len, SA_MAX_DECODE_TOKENS);
     if (num_splits < 0 || num_splits > kMaxSplits)
         return fail(SA_ERR_INVALID_ARG, "num_splits %d outside [0, %d]", num_splits, kMaxSplits);
     if (batch > 0 && !out)
         return fail(SA_ERR_INVALID_ARG, "out is NULL");
     if (out && !aligned16(out))
         return fail(SA_ERR_UNSUPPORTED, "out must be 16-byte aligned");
+    if (static_cast<int64_t>(batch) * q_len > 65535 * 8)
+        return fail(SA_ERR_UNSUPPORTED, "batch * q_len too large");
     if (batch == 0)
         return SA_OK;
+    const int32_t rows = batch * q_len;
     const int32_t S =
         num_splits == 0 ? sa_decode_num_splits(batch, kv->num_kv_heads, max_kv_len, window) : num_splits;
     if (S <= 1)
-        return launch_decode_kernel(q, kv, seqlens, batch, num_qo_heads, max_kv_len, sinks, window, sm_scale, out,
-                                    lse, nullptr, nullptr, 1, false, stream);
-    const size_t need = partial_bytes(S, batch, num_qo_heads, kv->head_dim);
+        return launch_decode_kernel(q, q_len, kv, seqlens, batch, num_qo_heads, max_kv_len, sinks, window,
+                                    sm_scale, out, lse, nullptr, nullptr, 1, false, stream);
+    const size_t need = partial_bytes(S, rows, num_qo_heads, kv->head_dim);
     if (!workspace || workspace_bytes < need)
         return fail(SA_ERR_WORKSPACE, "split decode (%d chunks) needs %zu workspace bytes, got %zu", S, need,
                     workspace ? workspace_bytes : size_t(0));
@@ -408,13 +419,44 @@ sa_status_t sa_decode(const void *q, const sa_kv_desc_t *kv, const int32_t *seql
         return fail(SA_ERR_UNSUPPORTED, "workspace must be 16-byte aligned");
     float *o_part = static_cast<float *>(workspace);
     float *lse_part = reinterpret_cast<float *>(static_cast<char *>(workspace) +
-                                                align256(static_cast<size_t>(S) * batch * num_qo_heads *
+                                                align256(static_cast<size_t>(S) * rows * num_qo_heads *
                                                          kv->head_dim * sizeof(float)));
-    st = launch_decode_kernel(q, kv, seqlens, batch, num_qo_heads, max_kv_len, nullptr, window, sm_scale, nullptr,
-                              nullptr, o_part, lse_part, S, true, stream);
+    st = launch_decode_kernel(q, q_len, kv, seqlens, batch, num_qo_heads, max_kv_len, nullptr, window, sm_scale,
+                              nullptr, nullptr, o_part, lse_part, S, true, stream);
     if (st != SA_OK)
         return st;
-    return sa_merge_states(o_part, lse_part, S, batch, num_qo_heads, kv->head_dim, sinks, out, lse, stream);
+    return sa_merge_states(o_part, lse_part, S, rows, num_qo_heads, kv->head_dim, sinks, out, lse, stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+sa_status_t sa_decode(const void *q, const sa_kv_desc_t *kv, const int32_t *seqlens, int32_t batch,
+                      int32_t num_qo_heads, int32_t max_kv_len, const float *sinks, int32_t window,
+                      float sm_scale, void *out, float *lse, void *workspace, size_t workspace_bytes,
+                      int32_t num_splits, cudaStream_t stream)
+{
+    return decode_impl(q, 1, kv, seqlens, batch, num_qo_heads, max_kv_len, sinks, window, sm_scale, out, lse,
+                       workspace, workspace_bytes, num_splits, stream);
+}
+
+size_t sa_decode_multi_workspace_size(int32_t batch, int32_t q_len, int32_t num_qo_heads, int32_t num_kv_heads,
+                                      int32_t head_dim, int32_t max_kv_len, int32_t window, int32_t num_splits)
+{
+    if (batch <= 0 || q_len <= 0 || num_qo_heads <= 0 || head_dim <= 0 || num_splits < 0)
+        return 0;
+    const int32_t S = num_splits == 0 ? sa_decode_num_splits(batch, num_kv_heads, max_kv_len, window) : num_splits;
+    return S <= 1 ? 0 : partial_bytes(S, batch * q_len, num_qo_heads, head_dim);
+}
+
+sa_status_t sa_decode_multi(const void *q, int32_t q_len, const sa_kv_desc_t *kv, const int32_t *seqlens,
+                            int32_t batch, int32_t num_qo_heads, int32_t max_kv_len, const float *sinks,
+                            int32_t window, float sm_scale, void *out, float *lse, void *workspace,
+                            size_t workspace_bytes, int32_t num_splits, cudaStream_t stream)
+{
+    return decode_impl(q, q_len, kv, seqlens, batch, num_qo_heads, max_kv_len, sinks, window, sm_scale, out, lse,
+                       workspace, workspace_bytes, num_splits, stream);
 }
 
 sa_status_t sa_decode_partial(const void *q, const sa_kv_desc_t *kv, const int32_t *seqlens, int32_t batch,
@@ -433,8 +475,8 @@ sa_status_t sa_decode_partial(const void *q, const sa_kv_desc_t *kv, const int32
         return fail(SA_ERR_UNSUPPORTED, "o_part must be 16-byte aligned");
     if (batch == 0)
         return SA_OK;
-    return launch_decode_kernel(q, kv, seqlens, batch, num_qo_heads, max_kv_len, nullptr, window, sm_scale, nullptr,
-                                nullptr, o_part, lse_part, num_splits, true, stream);
+    return launch_decode_kernel(q, 1, kv, seqlens, batch, num_qo_heads, max_kv_len, nullptr, window, sm_scale,
+                                nullptr, nullptr, o_part, lse_part, num_splits, true, stream);
 }
 
 sa_status_t sa_merge_states(const float *o_part, const float *lse_part, int32_t num_splits, int32_t n,

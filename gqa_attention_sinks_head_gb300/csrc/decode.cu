@@ -32,6 +32,14 @@
 // code, see e4m3x2_to_f16x2_scaled), the products run as f16 mma, and
 // 2^8 * k_scale (resp. 2^8 * v_scale) is folded into the score scale (resp.
 // the output scale).  Q is rounded to f16 for that path.
+//
+// Multi-token decode (q_len 2..8 new tokens per sequence, as a speculative or
+// multi-token-prediction verifier sends them; "GPT-OSS on day 0", the engine's
+// speculative and MTP decoders): token k of sequence b sits at position
+// L_b - q_len + k.  Each consumer warp owns one token (q_len <= 4; the warps
+// that share a token take turns over the tiles of a stage) or two (q_len 5..8,
+// TPW = 2; every warp then reads all four tiles of a stage), so the block still
+// reads each K/V byte of the kv head once for all tokens and heads.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -59,20 +67,18 @@ struct DecodeCfg {
     static constexpr int kTileBytes = kTile * kRowBytes;        // 1 KB or 2 KB
 };
 
+constexpr int kMaxTPW = 2;  // query tokens per consumer warp (q_len <= 8)
+
 template <bool FP8, int kStages>
 struct DecodeSmem {
     // K and V tiles of each stage, one per consumer warp (1 KB aligned).
     uint8_t k[kStages][kConsumerWarps][DecodeCfg<FP8>::kTileBytes];
     uint8_t v[kStages][kConsumerWarps][DecodeCfg<FP8>::kTileBytes];
-    float red_m[kConsumerWarps][kMaxGroup];
-    float red_l[kConsumerWarps][kMaxGroup];
+    float red_m[kConsumerWarps][kMaxTPW][kMaxGroup];
+    float red_l[kConsumerWarps][kMaxTPW][kMaxGroup];
     uint64_t full[kStages];
     uint64_t empty[kStages];
 };
-// The per-warp O^T partials of the final merge reuse the K tiles.
-static_assert(sizeof(float) * kConsumerWarps * kHeadDim * kMaxGroup <=
-                  sizeof(uint8_t) * 2 * kConsumerWarps * DecodeCfg<true>::kTileBytes,
-              "merge scratch must fit in the K tiles of two stages");
 
 // Byte offset of 16-byte chunk `chunk` of row `row` in a swizzled tile.
 template <bool FP8>
@@ -84,14 +90,17 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk)
         return row * 128 + ((chunk ^ (row & 7)) << 4);
 }
 
-template <bool FP8, int kStages>
-__global__ void __launch_bounds__(kThreads, 4) decode_kernel(const __grid_constant__ CUtensorMap tmk,
-                                                             const __grid_constant__ CUtensorMap tmv,
-                                                             const DecodeParams p)
+template <bool FP8, int kStages, int TPW>
+__global__ void __launch_bounds__(kThreads, TPW == 1 ? 4 : 3) decode_kernel(const __grid_constant__ CUtensorMap tmk,
+                                                                          const __grid_constant__ CUtensorMap tmv,
+                                                                          const DecodeParams p)
 {
     using Cfg = DecodeCfg<FP8>;
     extern __shared__ uint8_t smem_raw[];
-    static_assert(kStages >= 2, "merge scratch needs two stages of K tiles");
+    // the per-warp O^T partials of the final merge reuse the K tiles
+    static_assert(sizeof(float) * kConsumerWarps * TPW * kHeadDim * kMaxGroup <=
+                      sizeof(uint8_t) * kStages * kConsumerWarps * Cfg::kTileBytes,
+                  "merge scratch must fit in the K tiles");
     DecodeSmem<FP8, kStages> &sm =
         *reinterpret_cast<DecodeSmem<FP8, kStages> *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
@@ -101,14 +110,18 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const __grid_consta
     const int g = blockIdx.y;
     const int b = blockIdx.z;
 
-    // ---- the block's key range ------------------------------------------
+    // ---- the block's key range: the union over its query tokens -----------
+    const int qlen = p.q_len;
     int L = __ldg(p.seqlens + b);
     if (L < 0 || L > p.max_kv_len) {
         if (threadIdx.x == 0)
             atomicOr(p.status, SA_DEVICE_SEQLEN_RANGE);
         L = min(max(L, 0), p.max_kv_len);
     }
-    const int lo = p.window > 0 ? max(0, L - p.window) : 0;       // first visible key
+    if (L > 0 && L < qlen && threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0)
+        atomicOr(p.status, SA_DEVICE_BAD_QLEN);  // tokens at negative positions see no key (L = 0: empty slot)
+    // token k sits at L - qlen + k and sees keys (pos - window, pos]
+    const int lo = p.window > 0 ? max(0, L - qlen + 1 - p.window) : 0;  // first key of token 0
     const int t_begin = (lo & ~(kTile - 1)) + kTile * p.tiles_per_split * split;  // tile-aligned
     const int t_first = max(t_begin, lo);
     const int t_end = min(L, t_begin + kTile * p.tiles_per_split);
@@ -124,15 +137,26 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const __grid_consta
     }
     __syncthreads();
 
-    // consumer state, kept past the role split for the block-level merge
-    float m[2] = {-INFINITY, -INFINITY};
-    float l[2] = {0.f, 0.f};
-    float o[4][4];
+    // Token slots of this consumer warp.  TPW 1: token warp % qlen, shared by
+    // `rep` warps that take the stage's tiles j with j % rep == warp / qlen.
+    // TPW 2: tokens warp and warp + 4, every tile of the stage.
+    const int tok0_w = TPW == 1 ? (qlen > 0 ? warp % qlen : 0) : warp;
+    const int rep = TPW == 1 ? (kConsumerWarps - 1 - tok0_w) / max(qlen, 1) + 1 : 1;
+    const int rep_idx = TPW == 1 ? warp / max(qlen, 1) : 0;
+    const int ntok = TPW == 1 ? 1 : (warp + 4 < qlen ? 2 : 1);
+
+    // consumer state (per token slot), kept past the role split for the block-level merge
+    float m[TPW][2], l[TPW][2], o[TPW][4][4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int tt = 0; tt < TPW; ++tt) {
+        m[tt][0] = m[tt][1] = -INFINITY;
+        l[tt][0] = l[tt][1] = 0.f;
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-            o[i][j] = 0.f;
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                o[tt][i][j] = 0.f;
+    }
     const int r = lane >> 2;  // mma row group: key r / r+8 of a tile; head r in the B operand
     const int c = lane & 3;   // mma column pair: heads 2c, 2c+1 of the accumulators
 
@@ -183,12 +207,21 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const __grid_consta
         // =================== consumers ======================================
         const int h0 = g * p.group;
 
-        // Q^T as the B operand (K dimension = head_dim, N = the group's heads).
-        uint32_t qf[4][2];
-        {
-            const __nv_bfloat16 *qrow = reinterpret_cast<const __nv_bfloat16 *>(p.q) +
-                                        (static_cast<int64_t>(b) * p.num_qo_heads + h0 + r) * kHeadDim;
-            const bool ok = r < p.group;
+        // Q^T as the B operand (K dimension = head_dim, N = the group's heads),
+        // and each token slot's visible key range within this chunk.
+        uint32_t qf[TPW][4][2];
+        int tf[TPW], te[TPW];
+#pragma unroll
+        for (int tt = 0; tt < TPW; ++tt) {
+            const int tok = tok0_w + 4 * tt;
+            const int hi_k = L - qlen + tok + 1;  // one past the token's own position
+            const int lo_k = p.window > 0 ? max(0, hi_k - p.window) : 0;
+            tf[tt] = max(t_first, lo_k);
+            te[tt] = min(t_end, hi_k);
+            const __nv_bfloat16 *qrow =
+                reinterpret_cast<const __nv_bfloat16 *>(p.q) +
+                ((static_cast<int64_t>(b) * qlen + min(tok, qlen - 1)) * p.num_qo_heads + h0 + r) * kHeadDim;
+            const bool ok = r < p.group && tt < ntok;
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
                 if constexpr (FP8) {
@@ -197,23 +230,27 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const __grid_consta
                     uint2 w = ok ? *reinterpret_cast<const uint2 *>(qrow + 16 * ks + 4 * c) : make_uint2(0, 0);
                     __nv_bfloat162 x01 = *reinterpret_cast<__nv_bfloat162 *>(&w.x);
                     __nv_bfloat162 x23 = *reinterpret_cast<__nv_bfloat162 *>(&w.y);
-                    qf[ks][0] = pack_f16(__bfloat162float(x01.x), __bfloat162float(x01.y));
-                    qf[ks][1] = pack_f16(__bfloat162float(x23.x), __bfloat162float(x23.y));
+                    qf[tt][ks][0] = pack_f16(__bfloat162float(x01.x), __bfloat162float(x01.y));
+                    qf[tt][ks][1] = pack_f16(__bfloat162float(x23.x), __bfloat162float(x23.y));
                 } else {
-                    qf[ks][0] = ok ? *reinterpret_cast<const uint32_t *>(qrow + 16 * ks + 2 * c) : 0u;
-                    qf[ks][1] = ok ? *reinterpret_cast<const uint32_t *>(qrow + 16 * ks + 2 * c + 8) : 0u;
+                    qf[tt][ks][0] = ok ? *reinterpret_cast<const uint32_t *>(qrow + 16 * ks + 2 * c) : 0u;
+                    qf[tt][ks][1] = ok ? *reinterpret_cast<const uint32_t *>(qrow + 16 * ks + 2 * c + 8) : 0u;
                 }
             }
         }
 
-        // Running state for heads 2c, 2c+1 (m in base 2; l a per-lane partial sum).
-        if (!p.partial && warp == 0 && p.sinks) {
+        // Running state for heads 2c, 2c+1 (m in base 2; l a per-lane partial
+        // sum).  The sink seeds one warp per token (the first that holds it).
+        if (!p.partial && rep_idx == 0 && p.sinks) {
 #pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const int n = 2 * c + j;
-                if (n < p.group) {
-                    m[j] = __ldg(p.sinks + h0 + n) * kLog2e;  // m starts at the sink ...
-                    l[j] = (r == 0) ? 1.f : 0.f;              // ... and d at 1 (counted once)
+            for (int tt = 0; tt < TPW; ++tt) {
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int n = 2 * c + j;
+                    if (n < p.group && tt < ntok) {
+                        m[tt][j] = __ldg(p.sinks + h0 + n) * kLog2e;  // m starts at the sink ...
+                        l[tt][j] = (r == 0) ? 1.f : 0.f;              // ... and d at 1 (counted once)
+                    }
                 }
             }
         }
@@ -223,115 +260,126 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const __grid_consta
             const int buf = st % kStages;
             if (!mbar_wait(&sm.full[buf], (st / kStages) & 1, p.status))
                 break;
-            const int tile = st * kConsumerWarps + warp;
-            if (tile < ntiles) {
+            for (int j = rep_idx; j < kConsumerWarps; j += rep) {
+                const int tile = st * kConsumerWarps + j;
+                if (tile >= ntiles)
+                    break;
                 const int tok0 = t_begin + tile * kTile;
-                const uint32_t kt = smem_u32(sm.k[buf][warp]);
-                const uint32_t vt = smem_u32(sm.v[buf][warp]);
+                const uint32_t kt = smem_u32(sm.k[buf][j]);
+                const uint32_t vt = smem_u32(sm.v[buf][j]);
+#pragma unroll
+                for (int tt = 0; tt < TPW; ++tt) {
+                    if (tt >= ntok || tok0 + kTile <= tf[tt] || tok0 >= te[tt])
+                        continue;  // no key of this tile is visible to the token
+                    const int t_first = tf[tt], t_end = te[tt];
+                    float (&mm)[2] = m[tt];
+                    float (&ll)[2] = l[tt];
+                    float (&oo)[4][4] = o[tt];
 
-                // ---- S^T = K . Q^T  (16 keys x 8 heads, fp32) --------------
-                float s[4] = {0.f, 0.f, 0.f, 0.f};
-                if constexpr (FP8) {
+                    // ---- S^T = K . Q^T  (16 keys x 8 heads, fp32) --------------
+                    float s[4] = {0.f, 0.f, 0.f, 0.f};
+                    if constexpr (FP8) {
 #pragma unroll
-                    for (int j2 = 0; j2 < 2; ++j2) {
-                        uint32_t R0, R1, R2, R3;
-                        ldsm_x4(kt + swz<true>((mi & 1) * 8 + lr, 2 * j2 + (mi >> 1)), R0, R1, R2, R3);
-                        mma_f16(s, e4m3x2_to_f16x2_scaled<kSel01>(R0), e4m3x2_to_f16x2_scaled<kSel01>(R1),
-                                e4m3x2_to_f16x2_scaled<kSel23>(R0), e4m3x2_to_f16x2_scaled<kSel23>(R1),
-                                qf[2 * j2][0], qf[2 * j2][1]);
-                        mma_f16(s, e4m3x2_to_f16x2_scaled<kSel01>(R2), e4m3x2_to_f16x2_scaled<kSel01>(R3),
-                                e4m3x2_to_f16x2_scaled<kSel23>(R2), e4m3x2_to_f16x2_scaled<kSel23>(R3),
-                                qf[2 * j2 + 1][0], qf[2 * j2 + 1][1]);
-                    }
-                } else {
+                        for (int j2 = 0; j2 < 2; ++j2) {
+                            uint32_t R0, R1, R2, R3;
+                            ldsm_x4(kt + swz<true>((mi & 1) * 8 + lr, 2 * j2 + (mi >> 1)), R0, R1, R2, R3);
+                            mma_f16(s, e4m3x2_to_f16x2_scaled<kSel01>(R0), e4m3x2_to_f16x2_scaled<kSel01>(R1),
+                                    e4m3x2_to_f16x2_scaled<kSel23>(R0), e4m3x2_to_f16x2_scaled<kSel23>(R1),
+                                    qf[tt][2 * j2][0], qf[tt][2 * j2][1]);
+                            mma_f16(s, e4m3x2_to_f16x2_scaled<kSel01>(R2), e4m3x2_to_f16x2_scaled<kSel01>(R3),
+                                    e4m3x2_to_f16x2_scaled<kSel23>(R2), e4m3x2_to_f16x2_scaled<kSel23>(R3),
+                                    qf[tt][2 * j2 + 1][0], qf[tt][2 * j2 + 1][1]);
+                        }
+                    } else {
 #pragma unroll
-                    for (int ks = 0; ks < 4; ++ks) {
-                        uint32_t a0, a1, a2, a3;
-                        ldsm_x4(kt + swz<false>((mi & 1) * 8 + lr, 2 * ks + (mi >> 1)), a0, a1, a2, a3);
-                        mma_bf16(s, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+                        for (int ks = 0; ks < 4; ++ks) {
+                            uint32_t a0, a1, a2, a3;
+                            ldsm_x4(kt + swz<false>((mi & 1) * 8 + lr, 2 * ks + (mi >> 1)), a0, a1, a2, a3);
+                            mma_bf16(s, a0, a1, a2, a3, qf[tt][ks][0], qf[tt][ks][1]);
+                        }
                     }
-                }
 
-                // ---- online softmax (base 2) -------------------------------
-                // s[0]: key r, head 2c   s[1]: key r, head 2c+1
-                // s[2]: key r+8, head 2c s[3]: key r+8, head 2c+1
+                    // ---- online softmax (base 2) -------------------------------
+                    // s[0]: key r, head 2c   s[1]: key r, head 2c+1
+                    // s[2]: key r+8, head 2c s[3]: key r+8, head 2c+1
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    s[i] *= p.score_scale;
-                const bool edge = tok0 < t_first || tok0 + kTile > t_end;
-                uint32_t vm01 = 0xffffffffu, vm23 = 0xffffffffu;
-                if (edge) {
-                    const bool v0 = tok0 + r >= t_first && tok0 + r < t_end;
-                    const bool v8 = tok0 + r + 8 >= t_first && tok0 + r + 8 < t_end;
-                    s[0] = v0 ? s[0] : -INFINITY;
-                    s[1] = v0 ? s[1] : -INFINITY;
-                    s[2] = v8 ? s[2] : -INFINITY;
-                    s[3] = v8 ? s[3] : -INFINITY;
-                    // value rows outside the range are zeroed (a NaN there must not leak via 0 * NaN)
-                    const int k0 = tok0 + 2 * c, k8 = tok0 + 2 * c + 8;
-                    vm01 = ((k0 >= t_first && k0 < t_end) ? 0x0000ffffu : 0u) |
-                           ((k0 + 1 >= t_first && k0 + 1 < t_end) ? 0xffff0000u : 0u);
-                    vm23 = ((k8 >= t_first && k8 < t_end) ? 0x0000ffffu : 0u) |
-                           ((k8 + 1 >= t_first && k8 + 1 < t_end) ? 0xffff0000u : 0u);
-                }
-                float mx0 = fmaxf(s[0], s[2]);
-                float mx1 = fmaxf(s[1], s[3]);
-#pragma unroll
-                for (int off = 4; off < 32; off <<= 1) {
-                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-                }
-                const float mn0 = fmaxf(m[0], mx0);
-                const float mn1 = fmaxf(m[1], mx1);
-                const float mu0 = mn0 == -INFINITY ? 0.f : mn0;  // nothing seen yet: keep exp2 finite
-                const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
-                const float al0 = ex2(m[0] - mu0);
-                const float al1 = ex2(m[1] - mu1);
-                const float p0 = ex2(s[0] - mu0);
-                const float p1 = ex2(s[1] - mu1);
-                const float p2 = ex2(s[2] - mu0);
-                const float p3 = ex2(s[3] - mu1);
-                l[0] = l[0] * al0 + (p0 + p2);
-                l[1] = l[1] * al1 + (p1 + p3);
-                m[0] = mn0;
-                m[1] = mn1;
-#pragma unroll
-                for (int mt = 0; mt < 4; ++mt) {
-                    o[mt][0] *= al0;
-                    o[mt][1] *= al1;
-                    o[mt][2] *= al0;
-                    o[mt][3] *= al1;
-                }
-                // P (key-major C layout) -> P^T as the B operand (K = keys, N = heads)
-                uint32_t pb0, pb1;
-                if constexpr (FP8) {
-                    pb0 = movmatrix_t(pack_f16(p0, p1));
-                    pb1 = movmatrix_t(pack_f16(p2, p3));
-                } else {
-                    pb0 = movmatrix_t(pack_bf16(p0, p1));
-                    pb1 = movmatrix_t(pack_bf16(p2, p3));
-                }
-
-                // ---- O^T += V^T . P^T ---------------------------------------
-                if constexpr (FP8) {
-#pragma unroll
-                    for (int j2 = 0; j2 < 2; ++j2) {
-                        uint32_t R0, R1, R2, R3;
-                        ldsm_x4_t(vt + swz<true>((mi & 1) * 8 + lr, 2 * j2 + (mi >> 1)), R0, R1, R2, R3);
-                        // rows of m-tile 2*j2 (+1): row r <-> dim 16ch + 2r, row r+8 <-> 16ch + 2r + 1
-                        mma_f16(o[2 * j2], e4m3x2_to_f16x2_scaled<kSel02>(R0) & vm01,
-                                e4m3x2_to_f16x2_scaled<kSel13>(R0) & vm01, e4m3x2_to_f16x2_scaled<kSel02>(R1) & vm23,
-                                e4m3x2_to_f16x2_scaled<kSel13>(R1) & vm23, pb0, pb1);
-                        mma_f16(o[2 * j2 + 1], e4m3x2_to_f16x2_scaled<kSel02>(R2) & vm01,
-                                e4m3x2_to_f16x2_scaled<kSel13>(R2) & vm01, e4m3x2_to_f16x2_scaled<kSel02>(R3) & vm23,
-                                e4m3x2_to_f16x2_scaled<kSel13>(R3) & vm23, pb0, pb1);
+                    for (int i = 0; i < 4; ++i)
+                        s[i] *= p.score_scale;
+                    const bool edge = tok0 < t_first || tok0 + kTile > t_end;
+                    uint32_t vm01 = 0xffffffffu, vm23 = 0xffffffffu;
+                    if (edge) {
+                        const bool v0 = tok0 + r >= t_first && tok0 + r < t_end;
+                        const bool v8 = tok0 + r + 8 >= t_first && tok0 + r + 8 < t_end;
+                        s[0] = v0 ? s[0] : -INFINITY;
+                        s[1] = v0 ? s[1] : -INFINITY;
+                        s[2] = v8 ? s[2] : -INFINITY;
+                        s[3] = v8 ? s[3] : -INFINITY;
+                        // value rows outside the range are zeroed (a NaN there must not leak via 0 * NaN)
+                        const int k0 = tok0 + 2 * c, k8 = tok0 + 2 * c + 8;
+                        vm01 = ((k0 >= t_first && k0 < t_end) ? 0x0000ffffu : 0u) |
+                               ((k0 + 1 >= t_first && k0 + 1 < t_end) ? 0xffff0000u : 0u);
+                        vm23 = ((k8 >= t_first && k8 < t_end) ? 0x0000ffffu : 0u) |
+                               ((k8 + 1 >= t_first && k8 + 1 < t_end) ? 0xffff0000u : 0u);
                     }
-                } else {
+                    float mx0 = fmaxf(s[0], s[2]);
+                    float mx1 = fmaxf(s[1], s[3]);
+#pragma unroll
+                    for (int off = 4; off < 32; off <<= 1) {
+                        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+                    }
+                    const float mn0 = fmaxf(mm[0], mx0);
+                    const float mn1 = fmaxf(mm[1], mx1);
+                    const float mu0 = mn0 == -INFINITY ? 0.f : mn0;  // nothing seen yet: keep exp2 finite
+                    const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
+                    const float al0 = ex2(mm[0] - mu0);
+                    const float al1 = ex2(mm[1] - mu1);
+                    const float p0 = ex2(s[0] - mu0);
+                    const float p1 = ex2(s[1] - mu1);
+                    const float p2 = ex2(s[2] - mu0);
+                    const float p3 = ex2(s[3] - mu1);
+                    ll[0] = ll[0] * al0 + (p0 + p2);
+                    ll[1] = ll[1] * al1 + (p1 + p3);
+                    mm[0] = mn0;
+                    mm[1] = mn1;
 #pragma unroll
                     for (int mt = 0; mt < 4; ++mt) {
-                        uint32_t a0, a1, a2, a3;
-                        ldsm_x4_t(vt + swz<false>((mi >> 1) * 8 + lr, 2 * mt + (mi & 1)), a0, a1, a2, a3);
-                        mma_bf16(o[mt], a0 & vm01, a1 & vm01, a2 & vm23, a3 & vm23, pb0, pb1);
+                        oo[mt][0] *= al0;
+                        oo[mt][1] *= al1;
+                        oo[mt][2] *= al0;
+                        oo[mt][3] *= al1;
+                    }
+                    // P (key-major C layout) -> P^T as the B operand (K = keys, N = heads)
+                    uint32_t pb0, pb1;
+                    if constexpr (FP8) {
+                        pb0 = movmatrix_t(pack_f16(p0, p1));
+                        pb1 = movmatrix_t(pack_f16(p2, p3));
+                    } else {
+                        pb0 = movmatrix_t(pack_bf16(p0, p1));
+                        pb1 = movmatrix_t(pack_bf16(p2, p3));
+                    }
+
+                    // ---- O^T += V^T . P^T ---------------------------------------
+                    if constexpr (FP8) {
+#pragma unroll
+                        for (int j2 = 0; j2 < 2; ++j2) {
+                            uint32_t R0, R1, R2, R3;
+                            ldsm_x4_t(vt + swz<true>((mi & 1) * 8 + lr, 2 * j2 + (mi >> 1)), R0, R1, R2, R3);
+                            // rows of m-tile 2*j2 (+1): row r <-> dim 16ch + 2r, row r+8 <-> 16ch + 2r + 1
+                            mma_f16(oo[2 * j2], e4m3x2_to_f16x2_scaled<kSel02>(R0) & vm01,
+                                    e4m3x2_to_f16x2_scaled<kSel13>(R0) & vm01, e4m3x2_to_f16x2_scaled<kSel02>(R1) & vm23,
+                                    e4m3x2_to_f16x2_scaled<kSel13>(R1) & vm23, pb0, pb1);
+                            mma_f16(oo[2 * j2 + 1], e4m3x2_to_f16x2_scaled<kSel02>(R2) & vm01,
+                                    e4m3x2_to_f16x2_scaled<kSel13>(R2) & vm01, e4m3x2_to_f16x2_scaled<kSel02>(R3) & vm23,
+                                    e4m3x2_to_f16x2_scaled<kSel13>(R3) & vm23, pb0, pb1);
+                        }
+                    } else {
+#pragma unroll
+                        for (int mt = 0; mt < 4; ++mt) {
+                            uint32_t a0, a1, a2, a3;
+                            ldsm_x4_t(vt + swz<false>((mi >> 1) * 8 + lr, 2 * mt + (mi & 1)), a0, a1, a2, a3);
+                            mma_bf16(oo[mt], a0 & vm01, a1 & vm01, a2 & vm23, a3 & vm23, pb0, pb1);
+                        }
                     }
                 }
             }
@@ -340,65 +388,74 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const __grid_consta
                 mbar_arrive(&sm.empty[buf]);
         }
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            l[j] += __shfl_xor_sync(0xffffffffu, l[j], 4);
-            l[j] += __shfl_xor_sync(0xffffffffu, l[j], 8);
-            l[j] += __shfl_xor_sync(0xffffffffu, l[j], 16);
-        }
+        for (int tt = 0; tt < TPW; ++tt)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                l[tt][j] += __shfl_xor_sync(0xffffffffu, l[tt][j], 4);
+                l[tt][j] += __shfl_xor_sync(0xffffffffu, l[tt][j], 8);
+                l[tt][j] += __shfl_xor_sync(0xffffffffu, l[tt][j], 16);
+            }
     }
     __syncthreads();  // every warp is done with the tiles: their K area holds the merge scratch
-    float *red_o = reinterpret_cast<float *>(&sm.k[0][0][0]);  // [warp][dim][head]
+    float *red_o = reinterpret_cast<float *>(&sm.k[0][0][0]);  // [warp][slot][dim][head]
     if (warp < kConsumerWarps) {
-        if (r == 0) {
-            sm.red_m[warp][2 * c] = m[0];
-            sm.red_m[warp][2 * c + 1] = m[1];
-            sm.red_l[warp][2 * c] = l[0];
-            sm.red_l[warp][2 * c + 1] = l[1];
-        }
-        float *w = red_o + warp * kHeadDim * kMaxGroup;
 #pragma unroll
-        for (int mt = 0; mt < 4; ++mt) {
-            const int dlo = FP8 ? 16 * mt + 2 * r : 16 * mt + r;
-            const int dhi = FP8 ? dlo + 1 : dlo + 8;
-            w[dlo * kMaxGroup + 2 * c] = o[mt][0];
-            w[dlo * kMaxGroup + 2 * c + 1] = o[mt][1];
-            w[dhi * kMaxGroup + 2 * c] = o[mt][2];
-            w[dhi * kMaxGroup + 2 * c + 1] = o[mt][3];
+        for (int tt = 0; tt < TPW; ++tt) {
+            if (r == 0) {
+                sm.red_m[warp][tt][2 * c] = m[tt][0];
+                sm.red_m[warp][tt][2 * c + 1] = m[tt][1];
+                sm.red_l[warp][tt][2 * c] = l[tt][0];
+                sm.red_l[warp][tt][2 * c + 1] = l[tt][1];
+            }
+            float *w = red_o + (warp * TPW + tt) * kHeadDim * kMaxGroup;
+#pragma unroll
+            for (int mt = 0; mt < 4; ++mt) {
+                const int dlo = FP8 ? 16 * mt + 2 * r : 16 * mt + r;
+                const int dhi = FP8 ? dlo + 1 : dlo + 8;
+                w[dlo * kMaxGroup + 2 * c] = o[tt][mt][0];
+                w[dlo * kMaxGroup + 2 * c + 1] = o[tt][mt][1];
+                w[dhi * kMaxGroup + 2 * c] = o[tt][mt][2];
+                w[dhi * kMaxGroup + 2 * c + 1] = o[tt][mt][3];
+            }
         }
     }
     __syncthreads();
 
-    // ---- merge the four warp states; thread t: head t/16, dims 4*(t%16).. ----
+    // ---- merge the warp states of each token; thread t: head t/16, dims 4*(t%16).. ----
     if (threadIdx.x < 128) {
         const int n = threadIdx.x >> 4;
         const int d0 = (threadIdx.x & 15) * 4;
-        if (n < p.group) {
+        for (int k = 0; k < qlen && n < p.group; ++k) {
+            // slots holding token k: TPW 1: warps w with w % qlen == k; TPW 2: (k % 4, k / 4)
+            const int w0 = TPW == 1 ? k : k % 4;
+            const int wstep = TPW == 1 ? qlen : kConsumerWarps;
+            const int tt = TPW == 1 ? 0 : k / 4;
             float M = -INFINITY;
-#pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w)
-                M = fmaxf(M, sm.red_m[w][n]);
+            for (int w = w0; w < kConsumerWarps; w += wstep)
+                M = fmaxf(M, sm.red_m[w][tt][n]);
             float Ls = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
             if (M != -INFINITY) {
-#pragma unroll
-                for (int w = 0; w < kConsumerWarps; ++w) {
-                    const float sc = ex2(sm.red_m[w][n] - M);
-                    Ls += sc * sm.red_l[w][n];
+                for (int w = w0; w < kConsumerWarps; w += wstep) {
+                    const float sc = ex2(sm.red_m[w][tt][n] - M);
+                    Ls += sc * sm.red_l[w][tt][n];
+                    const float *src = red_o + ((w * TPW + tt) * kHeadDim + d0) * kMaxGroup + n;
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
-                        acc[i] += sc * red_o[(w * kHeadDim + d0 + i) * kMaxGroup + n];
+                        acc[i] += sc * src[i * kMaxGroup];
                 }
             }
             const float inv = Ls > 0.f ? p.out_scale / Ls : 0.f;
             const float lse = Ls > 0.f ? (M + lg2(Ls)) * kLn2 : -INFINITY;
             const int h = g * p.group + n;
+            const int64_t qrow = static_cast<int64_t>(b) * qlen + k;  // row of token k
             if (p.partial) {
-                const int64_t row = (static_cast<int64_t>(split) * p.batch + b) * p.num_qo_heads + h;
+                const int64_t row = (static_cast<int64_t>(split) * p.batch * qlen + qrow) * p.num_qo_heads + h;
                 *reinterpret_cast<float4 *>(p.o_part + row * kHeadDim + d0) =
                     make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
                 if (d0 == 0)
                     p.lse_part[row] = lse;
             } else {
-                const int64_t row = static_cast<int64_t>(b) * p.num_qo_heads + h;
+                const int64_t row = qrow * p.num_qo_heads + h;
                 uint2 pk;
                 pk.x = pack_bf16(acc[0] * inv, acc[1] * inv);
                 pk.y = pack_bf16(acc[2] * inv, acc[3] * inv);
@@ -419,7 +476,7 @@ size_t decode_smem_bytes()
     return sizeof(DecodeSmem<FP8, kStages>) + 1024;  // + slack for the 1 KB alignment
 }
 
-template <bool FP8, int kStages>
+template <bool FP8, int kStages, int TPW>
 cudaError_t prepare_decode()
 {
     // one cudaFuncSetAttribute per device and variant
@@ -430,7 +487,7 @@ cudaError_t prepare_decode()
         return e;
     if (dev >= 0 && dev < 64 && done[dev])
         return cudaSuccess;
-    e = cudaFuncSetAttribute(decode_kernel<FP8, kStages>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(decode_kernel<FP8, kStages, TPW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(decode_smem_bytes<FP8, kStages>()));
     if (e == cudaSuccess && dev >= 0 && dev < 64)
         done[dev] = 1;
@@ -440,21 +497,21 @@ cudaError_t prepare_decode()
 template <bool FP8, int kStages>
 cudaError_t occupancy_of(int *blocks_per_sm)
 {
-    cudaError_t e = prepare_decode<FP8, kStages>();
+    cudaError_t e = prepare_decode<FP8, kStages, 1>();
     if (e != cudaSuccess)
         return e;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, decode_kernel<FP8, kStages>, kThreads,
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, decode_kernel<FP8, kStages, 1>, kThreads,
                                                          decode_smem_bytes<FP8, kStages>());
 }
 
-template <bool FP8, int kStages>
+template <bool FP8, int kStages, int TPW>
 cudaError_t launch_of(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p, cudaStream_t stream)
 {
-    cudaError_t e = prepare_decode<FP8, kStages>();
+    cudaError_t e = prepare_decode<FP8, kStages, TPW>();
     if (e != cudaSuccess)
         return e;
     const dim3 grid(p.num_splits, p.num_kv_heads, p.batch);
-    decode_kernel<FP8, kStages><<<grid, kThreads, decode_smem_bytes<FP8, kStages>(), stream>>>(tk, tv, p);
+    decode_kernel<FP8, kStages, TPW><<<grid, kThreads, decode_smem_bytes<FP8, kStages>(), stream>>>(tk, tv, p);
     return cudaGetLastError();
 }
 
@@ -462,13 +519,18 @@ cudaError_t launch_of(const CUtensorMap &tk, const CUtensorMap &tv, const Decode
 
 cudaError_t decode_occupancy(bool fp8, int *blocks_per_sm)
 {
-    return fp8 ? occupancy_of<true, 2 * kDefaultStages>(blocks_per_sm) : occupancy_of<false, kDefaultStages>(blocks_per_sm);
+    return fp8 ? occupancy_of<true, 2 * kDefaultStages>(blocks_per_sm)
+               : occupancy_of<false, kDefaultStages>(blocks_per_sm);
 }
 
 cudaError_t launch_decode(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p, bool fp8,
                           cudaStream_t stream)
 {
-    return fp8 ? launch_of<true, 2 * kDefaultStages>(tk, tv, p, stream) : launch_of<false, kDefaultStages>(tk, tv, p, stream);
+    if (p.q_len > 4)  // two tokens per consumer warp
+        return fp8 ? launch_of<true, 2 * kDefaultStages, 2>(tk, tv, p, stream)
+                   : launch_of<false, kDefaultStages, 2>(tk, tv, p, stream);
+    return fp8 ? launch_of<true, 2 * kDefaultStages, 1>(tk, tv, p, stream)
+               : launch_of<false, kDefaultStages, 1>(tk, tv, p, stream);
 }
 
 }  // namespace sa

@@ -16,16 +16,17 @@ constexpr int kMaxGroup = 8;   // decode: query heads per kv head (mma N = 8)
 
 // Decode launch description (one call of sa_decode / sa_decode_partial).
 struct DecodeParams {
-    const void *q;             // bf16 [B, Hq, 64]
+    const void *q;             // bf16 [B * q_len, Hq, 64]
     const int32_t *seqlens;    // [B]
     const int32_t *page_table; // [B, table_stride] or nullptr
     const float *sinks;        // [Hq] or nullptr (final mode only)
-    void *out;                 // final: bf16 [B, Hq, 64]
-    float *lse;                // final: [B, Hq] or nullptr
-    float *o_part;             // partial: [S, B, Hq, 64]
-    float *lse_part;           // partial: [S, B, Hq]
+    void *out;                 // final: bf16 [B * q_len, Hq, 64]
+    float *lse;                // final: [B * q_len, Hq] or nullptr
+    float *o_part;             // partial: [S, B * q_len, Hq, 64]
+    float *lse_part;           // partial: [S, B * q_len, Hq]
     uint32_t *status;          // device status word
     int32_t batch, num_qo_heads, num_kv_heads, group;
+    int32_t q_len;             // query tokens per sequence (1..8), at positions L - q_len .. L - 1
     int32_t page_size, table_stride, num_pages, max_kv_len;
     int32_t window, num_splits, tiles_per_split;
     int32_t partial;           // 1: write sink-free partial states; 0: final output

@@ -109,7 +109,8 @@ typedef struct {
 #define SA_DEVICE_SEQLEN_RANGE 0x1u /* a seqlen was < 0 or > max_kv_len: clamped */
 #define SA_DEVICE_BAD_PAGE 0x2u     /* a page index outside [0, num_pages): read as zeros */
 #define SA_DEVICE_TIMEOUT 0x4u      /* a pipeline wait ran out its limit: output undefined */
-#define SA_DEVICE_BAD_QLEN 0x8u     /* prefill: a query length was < 0 or > L_kv or > max_q_len */
+#define SA_DEVICE_BAD_QLEN 0x8u     /* prefill: a query length was < 0 or > L_kv or > max_q_len;
+                                       multi-token decode: 0 < seqlens[b] < q_len */
 
 /*
  * sa_decode -- one query token per sequence against its paged KV cache.
@@ -161,6 +162,43 @@ int32_t sa_decode_num_splits(int32_t batch, int32_t num_kv_heads, int32_t max_kv
 size_t sa_decode_workspace_size(int32_t batch, int32_t num_qo_heads, int32_t num_kv_heads,
                                 int32_t head_dim, int32_t max_kv_len, int32_t window,
                                 int32_t num_splits);
+
+/*
+ * sa_decode_multi -- q_len (1..SA_MAX_DECODE_TOKENS) new query tokens per
+ * sequence against its paged KV cache, for example the draft tokens a
+ * speculative or multi-token-prediction decoder asks the model to verify
+ * ("GPT-OSS on day 0": the engine's speculative and MTP decoders).  Each block
+ * reads a kv head's keys once for every token and query head of the group.
+ *   q          device bf16 [batch * q_len, num_qo_heads, 64]; row b * q_len + k
+ *              is token k of sequence b, at position seqlens[b] - q_len + k
+ *              (all q_len tokens' keys are already in the cache), so token k
+ *              sees keys <= its position (and, with a window, the w most recent)
+ *   out, lse   device bf16 [batch * q_len, num_qo_heads, 64] / fp32
+ *              [batch * q_len, num_qo_heads] or NULL, rows as q
+ *   workspace  at least sa_decode_multi_workspace_size(...) bytes when split
+ *   other arguments as sa_decode; q_len = 1 is sa_decode.
+ * A sequence with 0 < seqlens[b] < q_len sets SA_DEVICE_BAD_QLEN; its tokens
+ * at negative positions see no key (out = 0, lse = sink).  seqlens[b] = 0
+ * marks an empty slot: every token of it gives out = 0, lse = sink, unflagged.
+ * Returns SA_OK, SA_ERR_INVALID_ARG, SA_ERR_UNSUPPORTED (q_len outside
+ * [1, SA_MAX_DECODE_TOKENS]), SA_ERR_WORKSPACE or SA_ERR_CUDA.
+ */
+#define SA_MAX_DECODE_TOKENS 8
+sa_status_t sa_decode_multi(const void *q, int32_t q_len, const sa_kv_desc_t *kv,
+                            const int32_t *seqlens, int32_t batch, int32_t num_qo_heads,
+                            int32_t max_kv_len, const float *sinks, int32_t window,
+                            float sm_scale, void *out, float *lse, void *workspace,
+                            size_t workspace_bytes, int32_t num_splits, cudaStream_t stream);
+
+/*
+ * Workspace bytes sa_decode_multi needs (the chunk count is that of
+ * sa_decode_num_splits for num_splits = 0).  Layout when S > 1: fp32 o_part
+ * [S, batch * q_len, num_qo_heads, head_dim] followed (at a 256-byte aligned
+ * offset) by fp32 lse_part [S, batch * q_len, num_qo_heads].
+ */
+size_t sa_decode_multi_workspace_size(int32_t batch, int32_t q_len, int32_t num_qo_heads,
+                                      int32_t num_kv_heads, int32_t head_dim, int32_t max_kv_len,
+                                      int32_t window, int32_t num_splits);
 
 /*
  * sa_decode_partial -- the first half of a split decode, exposed for callers

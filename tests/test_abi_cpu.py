@@ -127,3 +127,32 @@ def test_split_heuristic_is_deterministic_and_bounded(lib):
         assert s == lib.sa_decode_num_splits(*args)
     assert lib.sa_decode_num_splits(256, 8, 8192, 128) <= 2   # a 128-key window needs no split
     assert lib.sa_decode_num_splits(1, 8, 32768, 0) > 8        # one long sequence is spread out
+
+
+def _decode_multi(lib, d, q_len, **kw):
+    L = lib.load()
+    a = dict(q=4096, seqlens=512, batch=2, hq=64, maxlen=1000, sinks=None, window=0, scale=0.125, out=8192,
+             lse=None, ws=None, wsb=0, splits=1)
+    a.update(kw)
+    return L.sa_decode_multi(a["q"], q_len, ctypes.byref(d), a["seqlens"], a["batch"], a["hq"], a["maxlen"],
+                             a["sinks"], a["window"], a["scale"], a["out"], a["lse"], a["ws"], a["wsb"], a["splits"],
+                             None)
+
+
+@pytest.mark.parametrize("q_len,expect", [(0, 2), (-1, 2), (9, 2), (64, 2)])
+def test_decode_multi_token_count(lib, q_len, expect):
+    assert _decode_multi(lib, _desc(lib), q_len) == expect
+    assert "q_len" in lib.load().sa_last_error().decode()
+
+
+def test_decode_multi_validation_matches_decode(lib):
+    # the shared checks run first: a bad cache is refused whatever q_len is
+    assert _decode_multi(lib, _desc(lib, head_dim=128), 4) == 2
+    assert _decode_multi(lib, _desc(lib), 4, splits=4, ws=None, wsb=0) == 3
+    assert _decode_multi(lib, _desc(lib), 4, batch=0, q=None, seqlens=None, out=None) == 0
+
+
+def test_decode_multi_workspace_size(lib):
+    assert lib.sa_decode_multi_workspace_size(4, 3, 64, 8, 64, 1000, 0, 1) == 0
+    s = lib.sa_decode_multi_workspace_size(4, 3, 64, 8, 64, 1000, 0, 5)
+    assert s == lib.sa_decode_workspace_size(12, 64, 8, 64, 1000, 0, 5)  # rows = batch * q_len

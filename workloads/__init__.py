@@ -278,6 +278,8 @@ def make_config(cfg: int, *, window: int = 0, device="cpu") -> Case:
        context, L_kv ~ U[2048, 16384] (P=16, permuted table, HND, 64 poison
        pages), bottom-right causal; window 0 or 128.
     7: workload 6 on an FP8-E4M3 cache (per-tensor scales).
+    8: multi-token decode: the cache of workload 2 (B=64, L_b ~ U[1024, 8192],
+       paged bf16) with 4 new query tokens per sequence at L_b - 4 .. L_b - 1.
     """
     seed = CONFIG_SEED + cfg
     if cfg == 1:
@@ -305,6 +307,11 @@ def make_config(cfg: int, *, window: int = 0, device="cpu") -> Case:
                                  poison_pages=64, seed=seed, device=device, kv_dtype=dt,
                                  name="chunked prefill B=8 Lq=1024 L_kv~U[2048,16384] paged P=16 %s w=%d"
                                  % (dt, window))
+    if cfg == 8:
+        kl = config_seqlens(2)
+        return make_prefill_case([4] * len(kl), kl, paged=True, page_size=16, layout="HND", window=window,
+                                 poison_pages=64, seed=seed, device=device,
+                                 name="multi-token decode B=64 q_len=4 L~U[1024,8192] paged P=16 bf16 w=%d" % window)
     raise ValueError(cfg)
 
 
