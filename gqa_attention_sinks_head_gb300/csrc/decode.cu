@@ -60,6 +60,7 @@ constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kDefaultStages = 3;
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kLog2e = 1.44269504088896340736f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 of the largest tolerated p
 
 template <bool FP8>
 struct DecodeCfg {
@@ -321,34 +322,45 @@ __global__ void __launch_bounds__(kThreads, TPW == 1 ? 4 : 3) decode_kernel(cons
                         vm23 = ((k8 >= t_first && k8 < t_end) ? 0x0000ffffu : 0u) |
                                ((k8 + 1 >= t_first && k8 + 1 < t_end) ? 0xffff0000u : 0u);
                     }
+                    // The running max moves only when some score of the tile exceeds it
+                    // by more than kRescaleThreshold (log2 units): p stays below 2^8,
+                    // the result is unchanged (numerator and denominator share m), and
+                    // most tiles skip the cross-lane max and the O rescale.
                     float mx0 = fmaxf(s[0], s[2]);
                     float mx1 = fmaxf(s[1], s[3]);
+                    // (-inf - -inf is NaN: a lane with nothing visible never asks)
+                    const bool grow = mx0 - mm[0] > kRescaleThreshold || mx1 - mm[1] > kRescaleThreshold;
+                    if (__any_sync(0xffffffffu, grow)) {
 #pragma unroll
-                    for (int off = 4; off < 32; off <<= 1) {
-                        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-                        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+                        for (int off = 4; off < 32; off <<= 1) {
+                            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+                        }
+                        const float mn0 = fmaxf(mm[0], mx0);
+                        const float mn1 = fmaxf(mm[1], mx1);
+                        // alpha = 0 from m = -inf (l and O are still 0); 1 while nothing is visible
+                        const float al0 = mn0 == -INFINITY ? 1.f : ex2(mm[0] - mn0);
+                        const float al1 = mn1 == -INFINITY ? 1.f : ex2(mm[1] - mn1);
+                        ll[0] *= al0;
+                        ll[1] *= al1;
+                        mm[0] = mn0;
+                        mm[1] = mn1;
+#pragma unroll
+                        for (int mt = 0; mt < 4; ++mt) {
+                            oo[mt][0] *= al0;
+                            oo[mt][1] *= al1;
+                            oo[mt][2] *= al0;
+                            oo[mt][3] *= al1;
+                        }
                     }
-                    const float mn0 = fmaxf(mm[0], mx0);
-                    const float mn1 = fmaxf(mm[1], mx1);
-                    const float mu0 = mn0 == -INFINITY ? 0.f : mn0;  // nothing seen yet: keep exp2 finite
-                    const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
-                    const float al0 = ex2(mm[0] - mu0);
-                    const float al1 = ex2(mm[1] - mu1);
+                    const float mu0 = mm[0] == -INFINITY ? 0.f : mm[0];  // keep exp2 finite
+                    const float mu1 = mm[1] == -INFINITY ? 0.f : mm[1];
                     const float p0 = ex2(s[0] - mu0);
                     const float p1 = ex2(s[1] - mu1);
                     const float p2 = ex2(s[2] - mu0);
                     const float p3 = ex2(s[3] - mu1);
-                    ll[0] = ll[0] * al0 + (p0 + p2);
-                    ll[1] = ll[1] * al1 + (p1 + p3);
-                    mm[0] = mn0;
-                    mm[1] = mn1;
-#pragma unroll
-                    for (int mt = 0; mt < 4; ++mt) {
-                        oo[mt][0] *= al0;
-                        oo[mt][1] *= al1;
-                        oo[mt][2] *= al0;
-                        oo[mt][3] *= al1;
-                    }
+                    ll[0] += p0 + p2;
+                    ll[1] += p1 + p3;
                     // P (key-major C layout) -> P^T as the B operand (K = keys, N = heads)
                     uint32_t pb0, pb1;
                     if constexpr (FP8) {
