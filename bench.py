@@ -34,7 +34,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "sink-attn decode HBM GB/s (% peak); prefill TFLOP/s (% bf16 tensor peak)"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-DEFAULT_STEPS = {1: 2000, 2: 2000, 3: 50, 4: 100, 5: 500, 6: 50, 7: 50, 8: 1000}
+DEFAULT_STEPS = {1: 2000, 2: 2000, 3: 50, 4: 100, 5: 500, 6: 50, 7: 50, 8: 1000, 9: 2000}
 
 
 # ------------------------------------------------------------------ helpers
@@ -200,11 +200,12 @@ def prefill_flops(q_lens, kv_lens, window, hq, dim):
 
 
 def windows_of(cfg):
-    return {1: [0], 2: [0, 128], 3: [0, 128], 4: [0], 5: [0, 128, 0, 128], 6: [0, 128], 7: [0, 128], 8: [0, 128]}[cfg]
+    return {1: [0], 2: [0, 128], 3: [0, 128], 4: [0], 5: [0, 128, 0, 128], 6: [0, 128], 7: [0, 128], 8: [0, 128], 9: [0]}[cfg]
 
 
 PREFILL_CONFIGS = (3, 6, 7)
 MULTI_CONFIGS = (8,)
+ROPE_CONFIGS = (9,)
 
 
 def workload_name(cfg):
@@ -220,6 +221,7 @@ def workload_name(cfg):
            "64q/8kv heads, D=64, step = w=0 call + w=128 call",
         8: "multi-token decode B=64, 4 new tokens each, L~U[1024,8192] paged P=16 bf16, 64q/8kv heads, D=64, "
            "step = w=0 call + w=128 call",
+        9: "YaRN RoPE of q/k + paged bf16 cache write for 8192 new tokens (one sequence), 64q/8kv heads, D=64",
     }[cfg]
 
 
@@ -457,7 +459,112 @@ class MultiDecodeBench:
             n, self.B, self.q_len, self.Hq)
 
 
+class RopeBench:
+    """One step = one sa_rope_append over 8192 new tokens of one sequence
+    (q/k/v of a prefill chunk) into a paged bf16 cache."""
+
+    T = 8192
+
+    def __init__(self, sa, cfg, device):
+        import torch
+        import workloads as W
+        self.sa, self.cfg, self.torch = sa, cfg, torch
+        g = torch.Generator(device="cpu").manual_seed(1009)
+        self.Hq, self.Hkv, self.D = 64, 8, 64
+        T = self.T
+        self.kv = W.make_kv([T], self.Hkv, self.D, 16, paged=True, poison_pages=64, seed=1009, device=device,
+                            layout="HND")
+        self.q = torch.randn(T, self.Hq, self.D, generator=g).to(torch.bfloat16).to(device)
+        self.k = torch.randn(T, self.Hkv, self.D, generator=g).to(torch.bfloat16).to(device)
+        self.v = torch.randn(T, self.Hkv, self.D, generator=g).to(torch.bfloat16).to(device)
+        self.seq = torch.zeros(T, dtype=torch.int32, device=device)
+        self.pos = torch.arange(T, dtype=torch.int32, device=device)
+        self.yarn = dict(theta=150000.0, factor=32.0, original_max_position=4096, beta_fast=32.0, beta_slow=1.0)
+        self.table = sa.sa_rope_yarn_table(T, **self.yarn).to(device)
+        self.q_out = torch.empty_like(self.q)
+        self.calls = [dict(window=0, S=1)]
+        # read q, k, v, positions, sequence ids and the table rows; write q_out and the cache rows
+        self.step_bytes = (2 * T * (self.Hq + 2 * self.Hkv) * self.D * 2 + 8 * T + T * self.D * 4)
+        self.calls[0]["bytes"] = self.step_bytes
+        self.kernels_per_step = 1
+        self.unit = "GB/s"
+        self.elem = 2
+        self.B = 1
+        self.maxlen = T
+        self.dtype_name = "bf16 (fp32 rotation)"
+        self.e2e_api = "sa_rope_append with pinned host q/k/v/positions in, rotated q back; cache resident"
+        self.oracle_cores = 1  # the rotary oracle is single-threaded numpy
+
+    def amount(self):
+        return self.step_bytes / 1e9
+
+    def run_call(self, cl, stream, ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        self.sa.sa_rope_append(self.q, self.k, self.v, self.seq, self.pos, self.table, self.kv, 1, self.q_out,
+                               stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+
+    def step(self, stream, evs=None):
+        self.run_call(self.calls[0], stream, None if evs is None else evs[0])
+
+    def dominant(self):
+        return 0, "rope_append_kernel", self.step_bytes
+
+    def e2e(self, stream, steps, warmup):
+        torch = self.torch
+        hs = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t.cpu()) for t in
+              (self.q, self.k, self.v, self.pos)]
+        hout = torch.empty(self.q_out.shape, dtype=torch.bfloat16, pin_memory=True)
+        h2d = sum(t.numel() * t.element_size() for t in hs)
+        d2h = hout.numel() * 2
+
+        def one():
+            for dev, host in zip((self.q, self.k, self.v, self.pos), hs):
+                dev.copy_(host, non_blocking=True)
+            self.run_call(self.calls[0], stream)
+            hout.copy_(self.q_out, non_blocking=True)
+
+        with torch.cuda.stream(stream):
+            for _ in range(warmup):
+                one()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(steps):
+                one()
+            e1.record(stream)
+            torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps, h2d, d2h
+
+    def oracle_sample(self, budget_s, max_seqs=None):
+        """The oracle's rotation + cache write of the first n tokens."""
+        import copy
+        import numpy as np
+        from oracle import rope as R
+        n = 256 if max_seqs is None else max(1, min(self.T, 32 * max_seqs))
+        kc = self.kv.k.cpu().view(self.torch.int16).numpy().view(np.uint16).copy()
+        vc = self.kv.v.cpu().view(self.torch.int16).numpy().view(np.uint16).copy()
+        d = self.kv.as_dict()
+        cache = dict(k=kc, v=vc, dtype="bf16", page_table=self.kv.page_table.cpu().numpy(),
+                     page_size=self.kv.page_size, stride_page=d["stride_page"], stride_head=d["stride_head"],
+                     stride_token=d["stride_token"], k_scale=1.0, v_scale=1.0)
+        q = self.q[:n].double().cpu().numpy()
+        k = self.k[:n].double().cpu().numpy()
+        v = self.v[:n].double().cpu().numpy()
+        seq = self.seq[:n].cpu().numpy()
+        pos = self.pos[:n].cpu().numpy()
+        t0 = time.time()
+        R.rope_append(q, k, v, seq, pos, self.yarn, cache)
+        dt = time.time() - t0
+        nbytes = self.step_bytes * n / self.T
+        return dt, nbytes, "%d of %d tokens, every head" % (n, self.T)
+
+
 def make_bench(sa, cfg, device):
+    if cfg in ROPE_CONFIGS:
+        return RopeBench(sa, cfg, device)
     if cfg in PREFILL_CONFIGS:
         return PrefillBench(sa, cfg, device)
     if cfg in MULTI_CONFIGS:
@@ -655,7 +762,7 @@ def run_native(args, world, rank, local):
             dt, nbytes, reps = dt + d1, nbytes + b1, reps + 1
         line["cpu_baseline"] = {"value": round(nbytes / (1e9 if wl.unit == "GB/s" else 1e12) / dt, 6),
                                 "unit": wl.unit,
-                                "cores": oracle.num_threads(), "kind": "oracle",
+                                "cores": getattr(wl, "oracle_cores", 0) or oracle.num_threads(), "kind": "oracle",
                                 "sample": "%s; timed %d times" % (desc, reps),
                                 "seconds": round(dt, 2)}
     if rank == 0:
@@ -692,7 +799,7 @@ def run_reference(args, world, rank, local):
     # size the per-step sample from a one-sequence pilot
     dt1, b1, _ = wl.oracle_sample(5.0, max_seqs=1)
     per_step = total_budget / max(1, steps + warmup)
-    n = max(1, min(wl.B if cfg not in PREFILL_CONFIGS else 4096, int(per_step / max(dt1, 1e-6))))
+    n = max(1, min(wl.B if cfg not in PREFILL_CONFIGS + ROPE_CONFIGS else 4096, int(per_step / max(dt1, 1e-6))))
     for _ in range(warmup):
         wl.oracle_sample(per_step, max_seqs=n)
     t0 = time.time()
@@ -709,7 +816,7 @@ def run_reference(args, world, rank, local):
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded), same bytes as the native arm",
         "config": {"workload": workload_name(cfg), "global_batch": wl.B, "seq_len_max": wl.maxlen},
         "impl": "reference",
-        "cpu_baseline": {"value": round(value, 4), "unit": wl.unit, "cores": oracle.num_threads(),
+        "cpu_baseline": {"value": round(value, 4), "unit": wl.unit, "cores": getattr(wl, "oracle_cores", 0) or oracle.num_threads(),
                          "kind": "oracle", "sample": desc},
         "e2e": {"value": round(value, 4), "unit": wl.unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -722,7 +829,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
-    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5, 6, 7, 8])
+    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5, 6, 7, 8, 9])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--budget-s", type=float, default=120.0,
                     help="reference arm: host seconds the whole --steps/--warmup run may take")

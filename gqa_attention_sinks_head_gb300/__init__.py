@@ -16,7 +16,8 @@ import os
 __all__ = [
     "SinkAttnError", "KVDesc", "load", "build", "sa_decode", "sa_decode_partial", "sa_merge_states",
     "sa_prefill", "sa_decode_static_workspace", "sa_decode_num_splits", "sa_decode_workspace_size", "sa_device_status", "sa_version",
-    "sa_decode_multi", "sa_decode_multi_workspace_size", "SA_MAX_DECODE_TOKENS",
+    "sa_decode_multi", "sa_decode_multi_workspace_size", "SA_MAX_DECODE_TOKENS", "sa_rope_yarn_table",
+    "sa_rope_append",
     "SA_KV_BF16", "SA_KV_FP8_E4M3", "kv_desc",
 ]
 
@@ -29,7 +30,8 @@ SA_DEVICE_SEQLEN_RANGE, SA_DEVICE_BAD_PAGE, SA_DEVICE_TIMEOUT, SA_DEVICE_BAD_QLE
 
 EXPORTS = ["sa_decode", "sa_decode_num_splits", "sa_decode_workspace_size", "sa_decode_partial",
            "sa_merge_states", "sa_prefill", "sa_device_status", "sa_status_string", "sa_last_error",
-           "sa_version", "sa_decode_static_workspace", "sa_decode_multi", "sa_decode_multi_workspace_size"]
+           "sa_version", "sa_decode_static_workspace", "sa_decode_multi", "sa_decode_multi_workspace_size",
+           "sa_rope_yarn_table", "sa_rope_append"]
 SA_MAX_DECODE_TOKENS = 8
 SA_STATIC_WORKSPACE_BYTES = 16 << 20
 
@@ -79,6 +81,9 @@ def load(path: str | None = None):
     lib.sa_decode_multi.argtypes = [P, i32, KP, P, i32, i32, i32, P, i32, f32, P, P, P, sz, i32, P]
     lib.sa_decode_multi_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32]
     lib.sa_decode_multi_workspace_size.restype = sz
+    dbl = ctypes.c_double
+    lib.sa_rope_yarn_table.argtypes = [P, i32, i32, dbl, dbl, i32, dbl, dbl]
+    lib.sa_rope_append.argtypes = [P, P, P, i32, i32, P, P, P, i32, KP, i32, P, P]
     lib.sa_decode_partial.argtypes = [P, KP, P, i32, i32, i32, i32, f32, i32, P, P, P]
     lib.sa_merge_states.argtypes = [P, P, i32, i32, i32, i32, P, P, P, P]
     lib.sa_prefill.argtypes = [P, P, i32, KP, P, i32, i32, i32, i32, P, i32, f32, P, P, P]
@@ -92,7 +97,7 @@ def load(path: str | None = None):
     lib.sa_last_error.restype = ctypes.c_char_p
     lib.sa_version.restype = ctypes.c_int
     for fn in ("sa_decode", "sa_decode_static_workspace", "sa_decode_partial", "sa_merge_states", "sa_prefill",
-               "sa_device_status", "sa_decode_multi"):
+               "sa_device_status", "sa_decode_multi", "sa_rope_yarn_table", "sa_rope_append"):
         getattr(lib, fn).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -183,6 +188,27 @@ def sa_decode_multi_workspace_size(batch, q_len, num_qo_heads, num_kv_heads, hea
                                    num_splits=0):
     return int(load().sa_decode_multi_workspace_size(int(batch), int(q_len), int(num_qo_heads), int(num_kv_heads),
                                                      int(head_dim), int(max_kv_len), int(window), int(num_splits)))
+
+
+def sa_rope_yarn_table(max_position, *, theta, factor, original_max_position, beta_fast, beta_slow, head_dim=64):
+    """The rotary table of sa_rope_append as a CPU float32 tensor [max_position, 64]
+    (fill on the host; move it to the device yourself)."""
+    import torch
+    t = torch.empty(int(max_position), int(head_dim), dtype=torch.float32)
+    _check(load().sa_rope_yarn_table(ctypes.c_void_p(t.data_ptr()), int(max_position), int(head_dim),
+                                     float(theta), float(factor), int(original_max_position), float(beta_fast),
+                                     float(beta_slow)))
+    return t
+
+
+def sa_rope_append(q, k, v, seq_ids, positions, table, kv, batch, q_out, stream=None):
+    """sa_rope_append on torch CUDA tensors: writes q_out and the cache of kv."""
+    lib = load()
+    desc, keep = kv_desc(kv)
+    T, Hq, _ = q.shape
+    _check(lib.sa_rope_append(_ptr(q), _ptr(k), _ptr(v), T, Hq, _ptr(seq_ids), _ptr(positions), _ptr(table),
+                              int(table.shape[0]), ctypes.byref(desc), int(batch), _ptr(q_out), _stream(stream)))
+    return q_out
 
 
 def sa_decode_static_workspace(q, kv, seqlens, sinks, window, sm_scale, out, lse=None, *, max_kv_len,

@@ -600,6 +600,111 @@ sa_status_t sa_prefill(const void *q, const int32_t *cu_seqlens_q, int32_t total
     return SA_OK;
 }
 
+sa_status_t sa_rope_yarn_table(float *table, int32_t max_position, int32_t head_dim, double theta,
+                               double factor, int32_t original_max_position, double beta_fast, double beta_slow)
+{
+    g_err[0] = 0;
+    if (!table || max_position < 1)
+        return fail(SA_ERR_INVALID_ARG, "table is NULL or max_position < 1");
+    if (head_dim != sa::kHeadDim)
+        return fail(SA_ERR_UNSUPPORTED, "head_dim %d: only 64 is supported", head_dim);
+    if (!std::isfinite(theta) || !(theta > 1.0) || !std::isfinite(factor) || original_max_position < 1 ||
+        !(beta_fast > 0.0) || !(beta_slow > 0.0) || !std::isfinite(beta_fast) || !std::isfinite(beta_slow))
+        return fail(SA_ERR_INVALID_ARG, "theta > 1, finite factor, original_max_position >= 1 and "
+                                        "beta_fast, beta_slow > 0 required");
+    constexpr int half = sa::kHeadDim / 2;
+    const double kPi = 3.14159265358979323846;
+    double freq[half];
+    double mscale = 1.0;
+    // the dimension index that turns n times over the original context
+    auto turns_dim = [&](double n) {
+        return sa::kHeadDim * std::log(original_max_position / (2.0 * kPi * n)) / (2.0 * std::log(theta));
+    };
+    double lo = 0.0, hi = 0.0;
+    if (factor > 1.0) {
+        lo = std::max(std::floor(turns_dim(beta_fast)), 0.0);
+        hi = std::min(std::ceil(turns_dim(beta_slow)), double(sa::kHeadDim - 1));
+        if (hi == lo)
+            hi = lo + 0.001;
+        mscale = 0.1 * std::log(factor) + 1.0;
+    }
+    for (int i = 0; i < half; ++i) {
+        const double f = std::pow(theta, -2.0 * i / sa::kHeadDim);
+        if (factor > 1.0) {
+            const double ramp = std::min(std::max((i - lo) / (hi - lo), 0.0), 1.0);
+            freq[i] = f * (1.0 - ramp) + (f / factor) * ramp;
+        } else {
+            freq[i] = f;
+        }
+    }
+    for (int64_t p = 0; p < max_position; ++p) {
+        float *row = table + p * sa::kHeadDim;
+        for (int i = 0; i < half; ++i) {
+            const double a = static_cast<double>(p) * freq[i];
+            row[i] = static_cast<float>(std::cos(a) * mscale);
+            row[half + i] = static_cast<float>(std::sin(a) * mscale);
+        }
+    }
+    return SA_OK;
+}
+
+sa_status_t sa_rope_append(const void *q, const void *k, const void *v, int32_t num_tokens, int32_t num_qo_heads,
+                           const int32_t *seq_ids, const int32_t *positions, const float *table,
+                           int32_t max_position, const sa_kv_desc_t *kv, int32_t batch, void *q_out,
+                           cudaStream_t stream)
+{
+    g_err[0] = 0;
+    if (num_tokens < 0 || batch < 0 || max_position < 1)
+        return fail(SA_ERR_INVALID_ARG, "num_tokens and batch must be >= 0, max_position >= 1");
+    sa_status_t st = check_kv(kv, batch, num_qo_heads, 0);
+    if (st != SA_OK)
+        return st;
+    if (num_tokens == 0)
+        return SA_OK;
+    if (!q || !k || !v || !seq_ids || !positions || !table || !q_out)
+        return fail(SA_ERR_INVALID_ARG, "q / k / v / seq_ids / positions / table / q_out is NULL");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(q_out) || !aligned16(table))
+        return fail(SA_ERR_UNSUPPORTED, "q, k, v, q_out and table must be 16-byte aligned");
+    if (static_cast<int64_t>(num_tokens) * (num_qo_heads + 2 * kv->num_kv_heads) >= (int64_t(1) << 37))
+        return fail(SA_ERR_UNSUPPORTED, "too many rows");
+    uint32_t *status = nullptr;
+    cudaError_t e = status_ptr(&status);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "device status word");
+    const bool fp8 = kv->dtype == SA_KV_FP8_E4M3;
+    sa::RopeParams p;
+    std::memset(&p, 0, sizeof p);
+    p.q = q;
+    p.k = k;
+    p.v = v;
+    p.seq_ids = seq_ids;
+    p.positions = positions;
+    p.table = table;
+    p.q_out = q_out;
+    p.k_cache = const_cast<void *>(kv->k);
+    p.v_cache = const_cast<void *>(kv->v);
+    p.page_table = kv->page_table;
+    p.status = status;
+    p.stride_page = kv->stride_page;
+    p.stride_head = kv->stride_head;
+    p.stride_token = kv->stride_token;
+    p.num_tokens = num_tokens;
+    p.num_qo_heads = num_qo_heads;
+    p.num_kv_heads = kv->num_kv_heads;
+    p.batch = batch;
+    p.max_position = max_position;
+    p.page_size = kv->page_size;
+    p.table_stride = kv->page_table_stride;
+    p.num_pages = kv->num_pages;
+    p.fp8 = fp8 ? 1 : 0;
+    p.k_inv_scale = fp8 ? 1.f / kv->k_scale : 1.f;
+    p.v_inv_scale = fp8 ? 1.f / kv->v_scale : 1.f;
+    e = sa::launch_rope_append(p, stream);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "rope_append launch");
+    return SA_OK;
+}
+
 sa_status_t sa_device_status(cudaStream_t stream, uint32_t *flags_out)
 {
     uint32_t *dptr = nullptr;

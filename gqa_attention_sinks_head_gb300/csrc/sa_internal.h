@@ -61,6 +61,23 @@ struct PrefillParams {
     float out_scale;                        // 1 (v_scale for an FP8 cache)
 };
 
+// Rotary embedding + cache append launch description.
+struct RopeParams {
+    const void *q, *k, *v;        // bf16 [T, Hq, 64], [T, Hkv, 64], [T, Hkv, 64]
+    const int32_t *seq_ids;       // [T]
+    const int32_t *positions;     // [T]
+    const float *table;           // [max_position, 64]: cos (scaled) in 0..31, sin (scaled) in 32..63
+    void *q_out;                  // bf16 [T, Hq, 64]
+    void *k_cache, *v_cache;      // written
+    const int32_t *page_table;    // [batch, table_stride] or nullptr (page = sequence)
+    uint32_t *status;
+    int64_t stride_page, stride_head, stride_token;  // elements
+    int32_t num_tokens, num_qo_heads, num_kv_heads, batch, max_position;
+    int32_t page_size, table_stride, num_pages;
+    int32_t fp8;                  // cache holds E4M3 codes
+    float k_inv_scale, v_inv_scale;  // FP8: 1 / k_scale, 1 / v_scale
+};
+
 // Record `fmt` as the calling thread's sa_last_error() message and return st.
 sa_status_t set_last_error(sa_status_t st, const char *fmt, ...);
 
@@ -69,6 +86,7 @@ cudaError_t launch_decode(const CUtensorMap &tk, const CUtensorMap &tv, const De
                           bool fp8, cudaStream_t stream);
 cudaError_t decode_occupancy(bool fp8, int *blocks_per_sm);
 cudaError_t launch_merge(const MergeParams &p, cudaStream_t stream);
+cudaError_t launch_rope_append(const RopeParams &p, cudaStream_t stream);
 cudaError_t launch_prefill(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                            const PrefillParams &p, bool fp8, cudaStream_t stream);
 

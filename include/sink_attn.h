@@ -111,6 +111,8 @@ typedef struct {
 #define SA_DEVICE_TIMEOUT 0x4u      /* a pipeline wait ran out its limit: output undefined */
 #define SA_DEVICE_BAD_QLEN 0x8u     /* prefill: a query length was < 0 or > L_kv or > max_q_len;
                                        multi-token decode: 0 < seqlens[b] < q_len */
+#define SA_DEVICE_BAD_TOKEN 0x10u   /* rope_append: a token's sequence id or position was out of
+                                       range (that token's rows were skipped) */
 
 /*
  * sa_decode -- one query token per sequence against its paged KV cache.
@@ -269,6 +271,59 @@ sa_status_t sa_prefill(const void *q, const int32_t *cu_seqlens_q, int32_t total
                        int32_t max_q_len, int32_t max_kv_len, const float *sinks,
                        int32_t window, float sm_scale, void *out, float *lse,
                        cudaStream_t stream);
+
+/*
+ * sa_rope_yarn_table -- fill a HOST buffer with the rotary table that
+ * sa_rope_append reads: for each position p in [0, max_position), 64 floats,
+ * cos(p * f_i) * mscale for i = 0..31 then sin(p * f_i) * mscale.
+ * Frequencies follow YaRN ("GPT-OSS on day 0": YaRN position encoding as in
+ * DeepSeek-V3), evaluated in double precision:
+ *   f_i = theta^(-i/32) blended with f_i / factor by a ramp over the
+ *   dimension index between floor(c(beta_fast)) and ceil(c(beta_slow)), where
+ *   c(n) = 64 ln(original_max_position / (2 pi n)) / (2 ln theta) is the
+ *   dimension that turns n times over the original context; dimensions below
+ *   the ramp keep f_i, those above it use f_i / factor.
+ *   mscale = 0.1 ln(factor) + 1 (1 when factor <= 1): q and k are both scaled,
+ *   so q.k grows by mscale^2.
+ * factor <= 1 gives plain rotary embeddings.  head_dim must be 64.
+ * Returns SA_OK or SA_ERR_INVALID_ARG (NULL table, max_position < 1, theta <= 1,
+ * original_max_position < 1, beta_fast <= 0, beta_slow <= 0, non-finite values)
+ * or SA_ERR_UNSUPPORTED (head_dim != 64).  Copy the buffer to the device.
+ */
+sa_status_t sa_rope_yarn_table(float *table, int32_t max_position, int32_t head_dim, double theta,
+                               double factor, int32_t original_max_position, double beta_fast,
+                               double beta_slow);
+
+/*
+ * sa_rope_append -- the step in front of attention for T new tokens (vLLM
+ * "GPT-OSS optimisations on NVIDIA Blackwell": RoPE, query and KV-cache
+ * write as one operator).  One pass over the inputs:
+ *   q_out[t, h] = rotate(q[t, h], positions[t])
+ *   cache K at (seq_ids[t], positions[t], g) = rotate(k[t, g], positions[t])
+ *   cache V at (seq_ids[t], positions[t], g) = v[t, g]
+ * where rotate mixes dims i and i + 32 with the table row of the position:
+ * (x_i c_i - x_{i+32} s_i, x_{i+32} c_i + x_i s_i).  The cache slot of
+ * sequence b at position p is page kv->page_table[b, p / page_size] (page b
+ * without a table), token slot p % page_size, in the descriptor's strides.
+ * An FP8 cache stores e4m3(value / scale) (k_scale, v_scale; round to nearest
+ * even, saturated to +-448); a bf16 cache the value rounded to nearest even.
+ *   q            device bf16 [num_tokens, num_qo_heads, 64]
+ *   k, v         device bf16 [num_tokens, kv->num_kv_heads, 64]
+ *   seq_ids      device int32 [num_tokens], each in [0, batch)
+ *   positions    device int32 [num_tokens], each in [0, max_position)
+ *   table        device fp32 [max_position, 64] from sa_rope_yarn_table
+ *   kv           the cache to write (kv->k and kv->v are written)
+ *   batch        rows of kv->page_table (sequences), or pages when it is NULL
+ *   q_out        device bf16 [num_tokens, num_qo_heads, 64] (may alias q)
+ * A token whose sequence id or position is out of range, or whose table entry
+ * lies past the table row, is skipped and sets SA_DEVICE_BAD_TOKEN; one whose
+ * page is outside [0, num_pages) is skipped and sets SA_DEVICE_BAD_PAGE.
+ * Returns SA_OK, SA_ERR_INVALID_ARG, SA_ERR_UNSUPPORTED or SA_ERR_CUDA.
+ */
+sa_status_t sa_rope_append(const void *q, const void *k, const void *v, int32_t num_tokens,
+                           int32_t num_qo_heads, const int32_t *seq_ids, const int32_t *positions,
+                           const float *table, int32_t max_position, const sa_kv_desc_t *kv,
+                           int32_t batch, void *q_out, cudaStream_t stream);
 
 /*
  * sa_decode_static_workspace -- sa_decode for callers that cannot allocate
