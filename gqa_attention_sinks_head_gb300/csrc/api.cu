@@ -665,8 +665,8 @@ sa_status_t sa_rope_append(const void *q, const void *k, const void *v, int32_t 
         return fail(SA_ERR_INVALID_ARG, "q / k / v / seq_ids / positions / table / q_out is NULL");
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(q_out) || !aligned16(table))
         return fail(SA_ERR_UNSUPPORTED, "q, k, v, q_out and table must be 16-byte aligned");
-    if (static_cast<int64_t>(num_tokens) * (num_qo_heads + 2 * kv->num_kv_heads) >= (int64_t(1) << 37))
-        return fail(SA_ERR_UNSUPPORTED, "too many rows");
+    if (static_cast<int64_t>(num_tokens) * (num_qo_heads + 2 * kv->num_kv_heads) >= (int64_t(1) << 31))
+        return fail(SA_ERR_UNSUPPORTED, "num_tokens * (num_qo_heads + 2 * num_kv_heads) must be below 2^31");
     uint32_t *status = nullptr;
     cudaError_t e = status_ptr(&status);
     if (e != cudaSuccess)

@@ -9,7 +9,8 @@
 // Memory-bound: every head row (one token's q, k or v of one head: 64 bf16)
 // is read once and written once.  Four threads share a row: thread s handles
 // dims 8s..8s+7 of the first half and the same dims of the second half, the
-// pairs the rotation mixes, with 16-byte loads and stores.  cos and sin come
+// pairs the rotation mixes, with 16-byte loads and stores; each thread takes
+// four rows and loads all of them before it stores any.  cos and sin come
 // from a table the host fills in double precision (sa_rope_yarn_table), so no
 // large-angle argument reduction runs in fp32 on the device.
 #include <cuda_bf16.h>
@@ -20,7 +21,8 @@
 namespace sa {
 namespace {
 
-constexpr int kRowsPerBlock = 64;
+constexpr int kRowsPerBlock = 64;  // rows one pass of the block covers (4 threads per row)
+constexpr int kRowsPerThread = 4;
 constexpr int kThreads = 4 * kRowsPerBlock;
 
 __device__ __forceinline__ void unpack8(const uint4 &w, float (&f)[8])
@@ -54,33 +56,14 @@ __device__ __forceinline__ uint2 pack8_e4m3(const float (&f)[8], float inv_scale
     return make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
 }
 
-__global__ void __launch_bounds__(kThreads) rope_append_kernel(const RopeParams p)
+// One head row: rotate (unless it is v) and store.  x1/x2 hold dims 8s..8s+7
+// of the two halves.
+__device__ __forceinline__ void finish_row(const RopeParams &p, int t, int j, int pos, int b, int sub, float (&x1)[8],
+                                           float (&x2)[8])
 {
-    const int sub = threadIdx.x & 3;
-    const int heads = p.num_qo_heads + 2 * p.num_kv_heads;
-    const int64_t row = static_cast<int64_t>(blockIdx.x) * kRowsPerBlock + (threadIdx.x >> 2);
-    if (row >= static_cast<int64_t>(p.num_tokens) * heads)
-        return;
-    const int t = static_cast<int>(row / heads);
-    const int j = static_cast<int>(row % heads);
-    const int pos = __ldg(p.positions + t);
-    const int b = __ldg(p.seq_ids + t);
-    if (pos < 0 || pos >= p.max_position || b < 0 || b >= p.batch) {
-        if (sub == 0 && j == 0)
-            atomicOr(p.status, SA_DEVICE_BAD_TOKEN);
-        return;
-    }
-    // the source row and what becomes of it
     const bool is_q = j < p.num_qo_heads;
     const bool is_v = j >= p.num_qo_heads + p.num_kv_heads;
     const int g = is_q ? 0 : (is_v ? j - p.num_qo_heads - p.num_kv_heads : j - p.num_qo_heads);
-    const __nv_bfloat16 *src =
-        is_q ? reinterpret_cast<const __nv_bfloat16 *>(p.q) + (static_cast<int64_t>(t) * p.num_qo_heads + j) * kHeadDim
-             : reinterpret_cast<const __nv_bfloat16 *>(is_v ? p.v : p.k) +
-                   (static_cast<int64_t>(t) * p.num_kv_heads + g) * kHeadDim;
-    float x1[8], x2[8];
-    unpack8(__ldg(reinterpret_cast<const uint4 *>(src + 8 * sub)), x1);
-    unpack8(__ldg(reinterpret_cast<const uint4 *>(src + kHeadDim / 2 + 8 * sub)), x2);
     if (!is_v) {
         const float4 *tab = reinterpret_cast<const float4 *>(p.table + static_cast<int64_t>(pos) * kHeadDim);
         const float4 c0 = __ldg(tab + 2 * sub), c1 = __ldg(tab + 2 * sub + 1);
@@ -128,12 +111,62 @@ __global__ void __launch_bounds__(kThreads) rope_append_kernel(const RopeParams 
     }
 }
 
+// Each thread takes kRowsPerThread rows, kRowsPerBlock apart, and issues all
+// their loads before the first store: more bytes in flight per thread.
+__global__ void __launch_bounds__(kThreads) rope_append_kernel(const RopeParams p)
+{
+    const int sub = threadIdx.x & 3;
+    const uint32_t heads = p.num_qo_heads + 2 * p.num_kv_heads;
+    const uint32_t nrows = static_cast<uint32_t>(p.num_tokens) * heads;  // < 2^31 (checked on the host)
+    const uint32_t row0 = blockIdx.x * (kRowsPerBlock * kRowsPerThread) + (threadIdx.x >> 2);
+    uint4 w1[kRowsPerThread], w2[kRowsPerThread];
+    int tt[kRowsPerThread], jj[kRowsPerThread], pp[kRowsPerThread], bb[kRowsPerThread];
+#pragma unroll
+    for (int r = 0; r < kRowsPerThread; ++r) {
+        const uint32_t row = row0 + r * kRowsPerBlock;
+        tt[r] = -1;
+        if (row >= nrows)
+            continue;
+        const int t = static_cast<int>(row / heads);
+        const int j = static_cast<int>(row - static_cast<uint32_t>(t) * heads);
+        const bool is_q = j < p.num_qo_heads;
+        const bool is_v = j >= p.num_qo_heads + p.num_kv_heads;
+        const int g = is_q ? 0 : (is_v ? j - p.num_qo_heads - p.num_kv_heads : j - p.num_qo_heads);
+        const __nv_bfloat16 *src =
+            is_q ? reinterpret_cast<const __nv_bfloat16 *>(p.q) +
+                       (static_cast<int64_t>(t) * p.num_qo_heads + j) * kHeadDim
+                 : reinterpret_cast<const __nv_bfloat16 *>(is_v ? p.v : p.k) +
+                       (static_cast<int64_t>(t) * p.num_kv_heads + g) * kHeadDim;
+        w1[r] = __ldg(reinterpret_cast<const uint4 *>(src + 8 * sub));
+        w2[r] = __ldg(reinterpret_cast<const uint4 *>(src + kHeadDim / 2 + 8 * sub));
+        tt[r] = t;
+        jj[r] = j;
+        pp[r] = __ldg(p.positions + t);
+        bb[r] = __ldg(p.seq_ids + t);
+    }
+#pragma unroll
+    for (int r = 0; r < kRowsPerThread; ++r) {
+        if (tt[r] < 0)
+            continue;
+        if (pp[r] < 0 || pp[r] >= p.max_position || bb[r] < 0 || bb[r] >= p.batch) {
+            if (sub == 0 && jj[r] == 0)
+                atomicOr(p.status, SA_DEVICE_BAD_TOKEN);
+            continue;
+        }
+        float x1[8], x2[8];
+        unpack8(w1[r], x1);
+        unpack8(w2[r], x2);
+        finish_row(p, tt[r], jj[r], pp[r], bb[r], sub, x1, x2);
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_rope_append(const RopeParams &p, cudaStream_t stream)
 {
     const int64_t rows = static_cast<int64_t>(p.num_tokens) * (p.num_qo_heads + 2 * p.num_kv_heads);
-    const int64_t blocks = (rows + kRowsPerBlock - 1) / kRowsPerBlock;
+    const int64_t per_block = static_cast<int64_t>(kRowsPerBlock) * kRowsPerThread;
+    const int64_t blocks = (rows + per_block - 1) / per_block;
     if (blocks == 0)
         return cudaSuccess;
     rope_append_kernel<<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(p);
