@@ -76,6 +76,8 @@ def _load():
             lib.sao_attend.restype = ctypes.c_int
             lib.sao_attend.argtypes = [P, ctypes.c_int32, ctypes.c_int32, P, P, ctypes.POINTER(_KV), P,
                                        P, ctypes.c_int32, ctypes.c_double, P, P, ctypes.c_int64, P, P]
+            lib.sao_attend_q8.restype = ctypes.c_int
+            lib.sao_attend_q8.argtypes = [P, ctypes.c_double] + lib.sao_attend.argtypes[1:]
             lib.sao_attend_range.restype = ctypes.c_int
             lib.sao_attend_range.argtypes = lib.sao_attend.argtypes[:13] + [ctypes.c_int32, ctypes.c_int32,
                                                                              P, P]
@@ -178,10 +180,11 @@ def prefill_rows(cu_seqlens_q, seqlens_kv):
 
 # ------------------------------------------------------------------ the math
 def attend(q, row_seq, row_pos, kv: dict, seqlens, sinks, window: int, sm_scale: float,
-           sel_rows=None, sel_heads=None, split=None, key_range=None):
+           sel_rows=None, sel_heads=None, split=None, key_range=None, q_scale=None):
     """out [n_sel, D] and lse [n_sel] (fp64) for the selected (row, head) pairs.
 
-    q: bf16 [n_rows, Hq, D]; kv: dict with k, v, dtype ('bf16' | 'e4m3'),
+    q: bf16 [n_rows, Hq, D], or E4M3 codes (uint8) when q_scale is given
+    (element = code * q_scale); kv: dict with k, v, dtype ('bf16' | 'e4m3'),
     num_pages, num_kv_heads, head_dim, page_size, strides (elements),
     page_table ([B, max_pages] int32 or None), k_scale, v_scale.
     sel_rows/sel_heads default to every (row, head).  split=(num_chunks, chunk)
@@ -191,7 +194,7 @@ def attend(q, row_seq, row_pos, kv: dict, seqlens, sinks, window: int, sm_scale:
     """
     lib = _load()
     keep = []
-    qa = _np(q).view(np.uint16)
+    qa = _np(q).view(np.uint8 if q_scale is not None else np.uint16)
     n_rows, Hq, D = qa.shape
     row_seq = _np(row_seq, np.int32)
     row_pos = _np(row_pos, np.int32)
@@ -206,7 +209,13 @@ def attend(q, row_seq, row_pos, kv: dict, seqlens, sinks, window: int, sm_scale:
     kvs = _kv_struct(kv, keep)
     out = np.zeros((n_sel, D), np.float64)
     lse = np.zeros((n_sel,), np.float64)
-    if key_range is not None:
+    if q_scale is not None:
+        if key_range is not None or split is not None:
+            raise ValueError("an E4M3 query is supported by the plain definition only")
+        rc = lib.sao_attend_q8(_ptr(qa), float(q_scale), n_rows, Hq, _ptr(row_seq), _ptr(row_pos),
+                               ctypes.byref(kvs), _ptr(seqlens), _ptr(sinks_a), int(window), float(sm_scale),
+                               _ptr(sel_rows), _ptr(sel_heads), n_sel, _ptr(out), _ptr(lse))
+    elif key_range is not None:
         rc = lib.sao_attend_range(_ptr(qa), n_rows, Hq, _ptr(row_seq), _ptr(row_pos), ctypes.byref(kvs),
                                   _ptr(seqlens), _ptr(sinks_a), int(window), float(sm_scale),
                                   _ptr(sel_rows), _ptr(sel_heads), n_sel, int(key_range[0]),

@@ -133,8 +133,22 @@ static int key_visible(int j, int p, int L, int window)
     return 1;
 }
 
+/* One query element: bf16 bits (q_fmt 0) or an E4M3 code times q_scale (q_fmt 1). */
+typedef struct {
+    const void *row;
+    int fmt;
+    double scale;
+} sao_qrow_t;
+
+static double q_elem(const sao_qrow_t *q, int d)
+{
+    if (q->fmt == 0)
+        return sao_bf16_to_f64(((const uint16_t *)q->row)[d]);
+    return sao_e4m3_to_f64(((const uint8_t *)q->row)[d]) * q->scale;
+}
+
 /* Score s_j for one (row, head): sm_scale * q . k_j, in fp64. */
-static double score(const uint16_t *qrow, const sao_kv_t *kv, int b, int g, int j,
+static double score(const sao_qrow_t *qrow, const sao_kv_t *kv, int b, int g, int j,
                     double sm_scale, int *err)
 {
     int64_t off = kv_offset(kv, b, g, j);
@@ -145,7 +159,7 @@ static double score(const uint16_t *qrow, const sao_kv_t *kv, int b, int g, int 
         return 0.0;
     }
     for (d = 0; d < kv->head_dim; ++d)
-        acc += sao_bf16_to_f64(qrow[d]) * kv_elem(kv, kv->k, kv->k_scale, off, d);
+        acc += q_elem(qrow, d) * kv_elem(kv, kv->k, kv->k_scale, off, d);
     return sm_scale * acc;
 }
 
@@ -154,7 +168,7 @@ static double score(const uint16_t *qrow, const sao_kv_t *kv, int b, int g, int 
  * of the causal/window set J.  with_sink selects whether sigma takes part.
  * Writes o[0..D) and *lse.  Two passes: all scores first, then max, then sums.
  */
-static int attend_one(const uint16_t *qrow, const sao_kv_t *kv, int b, int g, int p, int L,
+static int attend_one(const sao_qrow_t *qrow, const sao_kv_t *kv, int b, int g, int p, int L,
                       int window, double sm_scale, double sigma, int with_sink,
                       int j_lo, int j_hi, double *o, double *lse)
 {
@@ -231,9 +245,9 @@ static int attend_one(const uint16_t *qrow, const sao_kv_t *kv, int b, int g, in
  *   sel_row, sel_head [n_sel]; out [n_sel, head_dim] fp64; lse [n_sel] fp64
  * Returns 0, or nonzero on a page table that points outside the pool.
  */
-static int attend_sel(const uint16_t *q, int32_t num_qo_heads, const int32_t *row_seq,
-                      const int32_t *row_pos, const sao_kv_t *kv, const int32_t *seqlens,
-                      const float *sinks, int32_t window, double sm_scale,
+static int attend_sel(const void *q, int q_fmt, double q_scale, int32_t num_qo_heads,
+                      const int32_t *row_seq, const int32_t *row_pos, const sao_kv_t *kv,
+                      const int32_t *seqlens, const float *sinks, int32_t window, double sm_scale,
                       const int32_t *sel_row, const int32_t *sel_head, int64_t n_sel,
                       int32_t j_lo, int32_t j_hi, double *out, double *lse)
 {
@@ -246,8 +260,12 @@ static int attend_sel(const uint16_t *q, int32_t num_qo_heads, const int32_t *ro
         int r = sel_row[i], h = sel_head[i];
         int b = row_seq[r];
         double sigma = sinks ? (double)sinks[h] : -INFINITY;
-        const uint16_t *qrow = q + ((int64_t)r * num_qo_heads + h) * D;
-        bad |= attend_one(qrow, kv, b, h / G, row_pos[r], seqlens[b], window, sm_scale,
+        const int64_t qoff = ((int64_t)r * num_qo_heads + h) * D;
+        sao_qrow_t qrow;
+        qrow.row = q_fmt == 0 ? (const void *)((const uint16_t *)q + qoff) : (const void *)((const uint8_t *)q + qoff);
+        qrow.fmt = q_fmt;
+        qrow.scale = q_scale;
+        bad |= attend_one(&qrow, kv, b, h / G, row_pos[r], seqlens[b], window, sm_scale,
                           sigma, sinks != NULL, j_lo, j_hi, out + i * D, lse + i);
     }
     return bad;
@@ -261,7 +279,24 @@ int sao_attend(const uint16_t *q, int32_t n_rows, int32_t num_qo_heads,
                double *out, double *lse)
 {
     (void)n_rows;
-    return attend_sel(q, num_qo_heads, row_seq, row_pos, kv, seqlens, sinks, window, sm_scale,
+    return attend_sel(q, 0, 1.0, num_qo_heads, row_seq, row_pos, kv, seqlens, sinks, window, sm_scale,
+                      sel_row, sel_head, n_sel, 0, 0x7fffffff, out, lse);
+}
+
+/*
+ * sao_attend with the query given as E4M3 codes: element value = code *
+ * q_scale (vLLM "GPT-OSS optimisations on NVIDIA Blackwell": part of the
+ * attention runs in FP8).  Everything else is sao_attend.
+ */
+int sao_attend_q8(const uint8_t *q, double q_scale, int32_t n_rows, int32_t num_qo_heads,
+                  const int32_t *row_seq, const int32_t *row_pos,
+                  const sao_kv_t *kv, const int32_t *seqlens,
+                  const float *sinks, int32_t window, double sm_scale,
+                  const int32_t *sel_row, const int32_t *sel_head, int64_t n_sel,
+                  double *out, double *lse)
+{
+    (void)n_rows;
+    return attend_sel(q, 1, q_scale, num_qo_heads, row_seq, row_pos, kv, seqlens, sinks, window, sm_scale,
                       sel_row, sel_head, n_sel, 0, 0x7fffffff, out, lse);
 }
 
@@ -279,7 +314,7 @@ int sao_attend_range(const uint16_t *q, int32_t n_rows, int32_t num_qo_heads,
                      int32_t j_lo, int32_t j_hi, double *out, double *lse)
 {
     (void)n_rows;
-    return attend_sel(q, num_qo_heads, row_seq, row_pos, kv, seqlens, sinks, window, sm_scale,
+    return attend_sel(q, 0, 1.0, num_qo_heads, row_seq, row_pos, kv, seqlens, sinks, window, sm_scale,
                       sel_row, sel_head, n_sel, j_lo, j_hi, out, lse);
 }
 
@@ -360,12 +395,15 @@ int sao_attend_split(const uint16_t *q, int32_t n_rows, int32_t num_qo_heads,
         int b = row_seq[r], p = row_pos[r], L = seqlens[b];
         int first = window > 0 ? p - window + 1 : 0;
         int s;
-        const uint16_t *qrow = q + ((int64_t)r * num_qo_heads + h) * D;
+        sao_qrow_t qrow;
+        qrow.row = q + ((int64_t)r * num_qo_heads + h) * D;
+        qrow.fmt = 0;
+        qrow.scale = 1.0;
         if (first < 0)
             first = 0;
         for (s = 0; s < num_chunks; ++s) {
             int lo = first + s * chunk;
-            bad |= attend_one(qrow, kv, b, h / G, p, L, window, sm_scale, 0.0, 0,
+            bad |= attend_one(&qrow, kv, b, h / G, p, L, window, sm_scale, 0.0, 0,
                               lo, lo + chunk, part_o + ((int64_t)s * n_sel + i) * D,
                               part_lse + (int64_t)s * n_sel + i);
         }

@@ -400,3 +400,44 @@ def test_golden_worked_examples(oracle):
         exp_l = np.array([float(x) for x in c["expect_lse"]], np.float64)
         assert np.allclose(out, exp_o, atol=1e-15), c["name"]
         assert np.allclose(lse, exp_l, atol=1e-15), c["name"]
+
+
+# ------------------------------------------------------- E4M3 query input
+@pytest.mark.parametrize("kv_dtype", ["bf16", "e4m3"])
+def test_e4m3_query_equals_sdpa_on_decoded_values(oracle, kv_dtype):
+    """A query given as E4M3 codes * q_scale: the SDPA identity evaluated on
+    the codes decoded by torch (an independent decoder), for a scale that is
+    not a power of two."""
+    case = W.make_prefill_case([5, 33], [40, 33], window=16, kv_dtype=kv_dtype, num_qo_heads=4,
+                               num_kv_heads=2, seed=77)
+    q_scale = 0.0371
+    g = torch.Generator().manual_seed(78)
+    codes = torch.randint(0, 256, case.q.shape, generator=g, dtype=torch.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x11  # no NaN codes
+    rows = oracle.prefill_rows(case.cu_seqlens_q, case.seqlens)
+    out, lse = oracle.attend(codes, rows[0], rows[1], case.kv.as_dict(), case.seqlens, case.sinks, case.window,
+                             case.sm_scale, q_scale=q_scale)
+    decoded = codes.view(torch.float8_e4m3fn).double() * q_scale
+    ref_case = W.Case(decoded, case.kv, case.seqlens, case.sinks, case.window, case.sm_scale, case.cu_seqlens_q,
+                      "decoded")
+    ref_o, ref_l = sdpa_reference(ref_case, rows[0], rows[1])
+    n, Hq, D = case.q.shape
+    assert np.allclose(out.reshape(n, Hq, D), ref_o.numpy(), rtol=1e-10, atol=1e-10)
+    assert np.allclose(lse.reshape(n, Hq), ref_l.numpy(), rtol=1e-10, atol=1e-10)
+
+
+def test_e4m3_query_with_power_of_two_scale_equals_bf16_query(oracle):
+    """With q_scale = 2^-3 every decoded value is exact in bf16: the E4M3 path
+    and the bf16 path must then agree to the last bit."""
+    case = W.make_prefill_case([7], [20], seed=79)
+    g = torch.Generator().manual_seed(80)
+    codes = torch.randint(0, 256, case.q.shape, generator=g, dtype=torch.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x22
+    vals = codes.view(torch.float8_e4m3fn).float() * 0.125
+    q_bf16 = vals.to(torch.bfloat16)
+    assert torch.equal(q_bf16.float(), vals)
+    rows = oracle.prefill_rows(case.cu_seqlens_q, case.seqlens)
+    a = oracle.attend(codes, rows[0], rows[1], case.kv.as_dict(), case.seqlens, case.sinks, 0, case.sm_scale,
+                      q_scale=0.125)
+    b = oracle.attend(q_bf16, rows[0], rows[1], case.kv.as_dict(), case.seqlens, case.sinks, 0, case.sm_scale)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
