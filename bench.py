@@ -34,7 +34,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "sink-attn decode HBM GB/s (% peak); prefill TFLOP/s (% bf16 tensor peak)"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-DEFAULT_STEPS = {1: 2000, 2: 2000, 3: 50, 4: 100, 5: 500, 6: 50, 7: 50, 8: 1000, 9: 2000}
+DEFAULT_STEPS = {1: 2000, 2: 2000, 3: 50, 4: 100, 5: 500, 6: 50, 7: 50, 8: 1000, 9: 2000, 10: 50}
 
 
 # ------------------------------------------------------------------ helpers
@@ -200,10 +200,10 @@ def prefill_flops(q_lens, kv_lens, window, hq, dim):
 
 
 def windows_of(cfg):
-    return {1: [0], 2: [0, 128], 3: [0, 128], 4: [0], 5: [0, 128, 0, 128], 6: [0, 128], 7: [0, 128], 8: [0, 128], 9: [0]}[cfg]
+    return {1: [0], 2: [0, 128], 3: [0, 128], 4: [0], 5: [0, 128, 0, 128], 6: [0, 128], 7: [0, 128], 8: [0, 128], 9: [0], 10: [0, 128]}[cfg]
 
 
-PREFILL_CONFIGS = (3, 6, 7)
+PREFILL_CONFIGS = (3, 6, 7, 10)
 MULTI_CONFIGS = (8,)
 ROPE_CONFIGS = (9,)
 
@@ -222,6 +222,8 @@ def workload_name(cfg):
         8: "multi-token decode B=64, 4 new tokens each, L~U[1024,8192] paged P=16 bf16, 64q/8kv heads, D=64, "
            "step = w=0 call + w=128 call",
         9: "YaRN RoPE of q/k + paged bf16 cache write for 8192 new tokens (one sequence), 64q/8kv heads, D=64",
+        10: "workload 7 with E4M3 queries (sa_prefill_q8: FP8 tensor cores for Q K^T), step = w=0 call + "
+            "w=128 call",
     }[cfg]
 
 
@@ -579,9 +581,13 @@ class PrefillBench:
         import torch
         import workloads as W
         self.sa, self.cfg, self.torch = sa, cfg, torch
-        self.case = W.make_config(cfg, window=0, device=device)
+        self.q8 = cfg == 10
+        self.case = W.make_config(7 if self.q8 else cfg, window=0, device=device)
         c = self.case
         self.T, self.Hq, self.D = c.q.shape
+        if self.q8:  # per-tensor E4M3 codes of q (scale = amax / 448, nearest-even cast)
+            self.q_scale = float(c.q.float().abs().max()) / 448.0
+            self.q_codes = (c.q.float() / self.q_scale).to(torch.float8_e4m3fn).view(torch.uint8)
         self.Hkv = c.kv.num_kv_heads
         cu = c.cu_seqlens_q.cpu()
         self.q_lens = [int(x) for x in (cu[1:] - cu[:-1])]
@@ -597,6 +603,8 @@ class PrefillBench:
         self.unit = "TFLOP/s"
         self.elem = 1 if c.kv.dtype == "e4m3" else 2
         self.dtype_name = "bf16" if self.elem == 2 else "fp8-e4m3 kv (widened to f16 for the products), bf16 q/out"
+        if self.q8:
+            self.dtype_name = "fp8-e4m3 q and k (kind::f8f6f4 Q K^T), v widened to f16 for P V, bf16 out"
         self.e2e_api = "sa_prefill with pinned host q, k, v in, out/lse of both calls back"
         self.B = len(self.q_lens)
         self.maxlen = max(self.kv_lens)
@@ -608,8 +616,13 @@ class PrefillBench:
         c = self.case
         if ev is not None:
             ev[0].record(stream)
-        self.sa.sa_prefill(c.q, c.cu_seqlens_q, c.kv, c.seqlens, c.sinks, cl["window"], c.sm_scale, cl["out"],
-                           cl["lse"], max_q_len=max(self.q_lens), max_kv_len=self.maxlen, stream=stream)
+        if self.q8:
+            self.sa.sa_prefill_q8(self.q_codes, self.q_scale, c.cu_seqlens_q, c.kv, c.seqlens, c.sinks, cl["window"],
+                                  c.sm_scale, cl["out"], cl["lse"], max_q_len=max(self.q_lens),
+                                  max_kv_len=self.maxlen, stream=stream)
+        else:
+            self.sa.sa_prefill(c.q, c.cu_seqlens_q, c.kv, c.seqlens, c.sinks, cl["window"], c.sm_scale, cl["out"],
+                               cl["lse"], max_q_len=max(self.q_lens), max_kv_len=self.maxlen, stream=stream)
         if ev is not None:
             ev[1].record(stream)
 
@@ -623,16 +636,17 @@ class PrefillBench:
     def e2e(self, stream, steps, warmup):
         torch = self.torch
         c = self.case
-        hq = torch.empty(c.q.shape, dtype=c.q.dtype, pin_memory=True).copy_(c.q.cpu())
+        qdev = self.q_codes if self.q8 else c.q
+        hq = torch.empty(qdev.shape, dtype=qdev.dtype, pin_memory=True).copy_(qdev.cpu())
         hk = torch.empty(c.kv.k.shape, dtype=c.kv.k.dtype, pin_memory=True).copy_(c.kv.k.cpu())
         hv = torch.empty(c.kv.v.shape, dtype=c.kv.v.dtype, pin_memory=True).copy_(c.kv.v.cpu())
         houts = [(torch.empty(cl["out"].shape, dtype=torch.bfloat16, pin_memory=True),
                   torch.empty(cl["lse"].shape, dtype=torch.float32, pin_memory=True)) for cl in self.calls]
-        h2d = hq.numel() * 2 + (hk.numel() + hv.numel()) * hk.element_size()
+        h2d = hq.numel() * hq.element_size() + (hk.numel() + hv.numel()) * hk.element_size()
         d2h = sum(o.numel() * 2 + l.numel() * 4 for o, l in houts)
 
         def one():
-            c.q.copy_(hq, non_blocking=True)
+            qdev.copy_(hq, non_blocking=True)
             c.kv.k.copy_(hk, non_blocking=True)
             c.kv.v.copy_(hv, non_blocking=True)
             for cl, (ho, hl) in zip(self.calls, houts):
@@ -667,8 +681,12 @@ class PrefillBench:
         for cl in self.calls:
             sr = np.repeat(sel, self.Hq)
             sh = np.tile(np.arange(self.Hq, dtype=np.int32), len(sel))
-            oracle.attend(cpu.q, rows[0], rows[1], cpu.kv.as_dict(), cpu.seqlens, cpu.sinks, cl["window"],
-                          cpu.sm_scale, sr, sh)
+            if self.q8:
+                oracle.attend(self.q_codes.cpu(), rows[0], rows[1], cpu.kv.as_dict(), cpu.seqlens, cpu.sinks,
+                              cl["window"], cpu.sm_scale, sr, sh, q_scale=self.q_scale)
+            else:
+                oracle.attend(cpu.q, rows[0], rows[1], cpu.kv.as_dict(), cpu.seqlens, cpu.sinks, cl["window"],
+                              cpu.sm_scale, sr, sh)
             for r in sel:
                 p = int(rows[1][r])
                 nk = p + 1 if cl["window"] <= 0 else min(cl["window"], p + 1)
@@ -829,7 +847,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
-    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5, 6, 7, 8, 9])
+    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5, 6, 7, 8, 9, 10])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--budget-s", type=float, default=120.0,
                     help="reference arm: host seconds the whole --steps/--warmup run may take")

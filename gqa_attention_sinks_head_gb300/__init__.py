@@ -17,7 +17,7 @@ __all__ = [
     "SinkAttnError", "KVDesc", "load", "build", "sa_decode", "sa_decode_partial", "sa_merge_states",
     "sa_prefill", "sa_decode_static_workspace", "sa_decode_num_splits", "sa_decode_workspace_size", "sa_device_status", "sa_version",
     "sa_decode_multi", "sa_decode_multi_workspace_size", "SA_MAX_DECODE_TOKENS", "sa_rope_yarn_table",
-    "sa_rope_append",
+    "sa_rope_append", "sa_prefill_q8",
     "SA_KV_BF16", "SA_KV_FP8_E4M3", "kv_desc",
 ]
 
@@ -31,7 +31,7 @@ SA_DEVICE_SEQLEN_RANGE, SA_DEVICE_BAD_PAGE, SA_DEVICE_TIMEOUT, SA_DEVICE_BAD_QLE
 EXPORTS = ["sa_decode", "sa_decode_num_splits", "sa_decode_workspace_size", "sa_decode_partial",
            "sa_merge_states", "sa_prefill", "sa_device_status", "sa_status_string", "sa_last_error",
            "sa_version", "sa_decode_static_workspace", "sa_decode_multi", "sa_decode_multi_workspace_size",
-           "sa_rope_yarn_table", "sa_rope_append"]
+           "sa_rope_yarn_table", "sa_rope_append", "sa_prefill_q8"]
 SA_MAX_DECODE_TOKENS = 8
 SA_STATIC_WORKSPACE_BYTES = 16 << 20
 
@@ -83,7 +83,8 @@ def load(path: str | None = None):
     lib.sa_decode_multi_workspace_size.restype = sz
     dbl = ctypes.c_double
     lib.sa_rope_yarn_table.argtypes = [P, i32, i32, dbl, dbl, i32, dbl, dbl]
-    lib.sa_rope_append.argtypes = [P, P, P, i32, i32, P, P, P, i32, KP, i32, P, P]
+    lib.sa_rope_append.argtypes = [P, P, P, i32, i32, P, P, P, i32, KP, i32, P, f32, P]
+    lib.sa_prefill_q8.argtypes = [P, f32, P, i32, KP, P, i32, i32, i32, i32, P, i32, f32, P, P, P]
     lib.sa_decode_partial.argtypes = [P, KP, P, i32, i32, i32, i32, f32, i32, P, P, P]
     lib.sa_merge_states.argtypes = [P, P, i32, i32, i32, i32, P, P, P, P]
     lib.sa_prefill.argtypes = [P, P, i32, KP, P, i32, i32, i32, i32, P, i32, f32, P, P, P]
@@ -97,7 +98,7 @@ def load(path: str | None = None):
     lib.sa_last_error.restype = ctypes.c_char_p
     lib.sa_version.restype = ctypes.c_int
     for fn in ("sa_decode", "sa_decode_static_workspace", "sa_decode_partial", "sa_merge_states", "sa_prefill",
-               "sa_device_status", "sa_decode_multi", "sa_rope_yarn_table", "sa_rope_append"):
+               "sa_device_status", "sa_decode_multi", "sa_rope_yarn_table", "sa_rope_append", "sa_prefill_q8"):
         getattr(lib, fn).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -201,13 +202,15 @@ def sa_rope_yarn_table(max_position, *, theta, factor, original_max_position, be
     return t
 
 
-def sa_rope_append(q, k, v, seq_ids, positions, table, kv, batch, q_out, stream=None):
-    """sa_rope_append on torch CUDA tensors: writes q_out and the cache of kv."""
+def sa_rope_append(q, k, v, seq_ids, positions, table, kv, batch, q_out, q_out_scale=0.0, stream=None):
+    """sa_rope_append on torch CUDA tensors: writes q_out (bf16, or E4M3 codes
+    of q / q_out_scale when q_out_scale > 0) and the cache of kv."""
     lib = load()
     desc, keep = kv_desc(kv)
     T, Hq, _ = q.shape
     _check(lib.sa_rope_append(_ptr(q), _ptr(k), _ptr(v), T, Hq, _ptr(seq_ids), _ptr(positions), _ptr(table),
-                              int(table.shape[0]), ctypes.byref(desc), int(batch), _ptr(q_out), _stream(stream)))
+                              int(table.shape[0]), ctypes.byref(desc), int(batch), _ptr(q_out), float(q_out_scale),
+                              _stream(stream)))
     return q_out
 
 
@@ -251,6 +254,19 @@ def sa_prefill(q, cu_seqlens_q, kv, seqlens_kv, sinks, window, sm_scale, out, ls
                           Hq, int(max_q_len),
                           int(max_kv_len), _ptr(sinks), int(window), float(sm_scale), _ptr(out), _ptr(lse),
                           _stream(stream)))
+    return out, lse
+
+
+def sa_prefill_q8(q_codes, q_scale, cu_seqlens_q, kv, seqlens_kv, sinks, window, sm_scale, out, lse=None, *,
+                  max_q_len, max_kv_len, stream=None):
+    """sa_prefill with E4M3 query codes (uint8 [total_q, Hq, 64], value = code * q_scale)."""
+    lib = load()
+    desc, keep = kv_desc(kv)
+    B = int(seqlens_kv.shape[0])
+    Hq = int(q_codes.shape[1])
+    _check(lib.sa_prefill_q8(_ptr(q_codes), float(q_scale), _ptr(cu_seqlens_q), int(q_codes.shape[0]),
+                             ctypes.byref(desc), _ptr(seqlens_kv), B, Hq, int(max_q_len), int(max_kv_len),
+                             _ptr(sinks), int(window), float(sm_scale), _ptr(out), _ptr(lse), _stream(stream)))
     return out, lse
 
 

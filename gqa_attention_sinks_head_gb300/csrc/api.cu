@@ -511,10 +511,15 @@ sa_status_t sa_merge_states(const float *o_part, const float *lse_part, int32_t 
     return SA_OK;
 }
 
-sa_status_t sa_prefill(const void *q, const int32_t *cu_seqlens_q, int32_t total_q, const sa_kv_desc_t *kv,
-                       const int32_t *seqlens_kv, int32_t batch, int32_t num_qo_heads, int32_t max_q_len,
-                       int32_t max_kv_len, const float *sinks, int32_t window, float sm_scale, void *out,
-                       float *lse, cudaStream_t stream)
+}  // extern "C"
+
+namespace {
+
+// sa_prefill (bf16 q) and sa_prefill_q8 (E4M3 q codes, value = code * q_scale)
+sa_status_t prefill_impl(const void *q, bool q8, float q_scale, const int32_t *cu_seqlens_q, int32_t total_q,
+                         const sa_kv_desc_t *kv, const int32_t *seqlens_kv, int32_t batch, int32_t num_qo_heads,
+                         int32_t max_q_len, int32_t max_kv_len, const float *sinks, int32_t window,
+                         float sm_scale, void *out, float *lse, cudaStream_t stream)
 {
     g_err[0] = 0;
     if (batch < 0 || total_q < 0 || max_q_len < 0 || max_kv_len < 0 || window < 0)
@@ -540,6 +545,10 @@ sa_status_t sa_prefill(const void *q, const int32_t *cu_seqlens_q, int32_t total
     CUtensorMap tq, tk, tv;
     int dt = 0, dh = 0, dp = 0;
     const bool fp8 = kv->dtype == SA_KV_FP8_E4M3;
+    if (q8 && !fp8)
+        return fail(SA_ERR_UNSUPPORTED, "E4M3 queries need an FP8-E4M3 cache");
+    if (q8 && (!std::isfinite(q_scale) || q_scale == 0.f))
+        return fail(SA_ERR_INVALID_ARG, "q_scale must be finite and nonzero");
     st = encode_kv_map(&tk, kv->k, fp8, kv, 16, &dt, &dh, &dp);
     if (st != SA_OK)
         return st;
@@ -552,13 +561,15 @@ sa_status_t sa_prefill(const void *q, const int32_t *cu_seqlens_q, int32_t total
             return fail(SA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
         const cuuint64_t dims[3] = {static_cast<cuuint64_t>(sa::kHeadDim), static_cast<cuuint64_t>(num_qo_heads),
                                     static_cast<cuuint64_t>(total_q)};
-        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(sa::kHeadDim) * 2,
-                                       static_cast<cuuint64_t>(num_qo_heads) * sa::kHeadDim * 2};
+        const cuuint64_t esz = q8 ? 1 : 2;
+        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(sa::kHeadDim) * esz,
+                                       static_cast<cuuint64_t>(num_qo_heads) * sa::kHeadDim * esz};
         const cuuint32_t box[3] = {static_cast<cuuint32_t>(sa::kHeadDim), 1, 128};
         const cuuint32_t estr[3] = {1, 1, 1};
-        CUresult r = fn(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(q), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        CUresult r = fn(&tq, q8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                        const_cast<void *>(q), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        q8 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS)
             return fail(SA_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled rejected q (CUresult %d)", (int)r);
     }
@@ -589,15 +600,37 @@ sa_status_t sa_prefill(const void *q, const int32_t *cu_seqlens_q, int32_t total
     p.dim_token = dt;
     p.dim_head = dh;
     p.dim_page = dp;
-    // FP8: the kernel widens each code to its E4M3 value in f16
-    p.score_scale = sm_scale * kLog2e * (fp8 ? kv->k_scale : 1.f);
+    // FP8: the kernel widens each code to its E4M3 value in f16 (Q8: products of the codes)
+    p.score_scale = sm_scale * kLog2e * (fp8 ? kv->k_scale : 1.f) * (q8 ? q_scale : 1.f);
     p.out_scale = fp8 ? kv->v_scale : 1.f;
     if (p.num_q_tiles > 65535)
         return fail(SA_ERR_UNSUPPORTED, "max_q_len too large");
-    e = sa::launch_prefill(tq, tk, tv, p, fp8, stream);
+    e = sa::launch_prefill(tq, tk, tv, p, fp8, q8, stream);
     if (e != cudaSuccess)
         return cuda_fail(e, "prefill launch");
     return SA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+sa_status_t sa_prefill(const void *q, const int32_t *cu_seqlens_q, int32_t total_q, const sa_kv_desc_t *kv,
+                       const int32_t *seqlens_kv, int32_t batch, int32_t num_qo_heads, int32_t max_q_len,
+                       int32_t max_kv_len, const float *sinks, int32_t window, float sm_scale, void *out,
+                       float *lse, cudaStream_t stream)
+{
+    return prefill_impl(q, false, 1.f, cu_seqlens_q, total_q, kv, seqlens_kv, batch, num_qo_heads, max_q_len,
+                        max_kv_len, sinks, window, sm_scale, out, lse, stream);
+}
+
+sa_status_t sa_prefill_q8(const void *q, float q_scale, const int32_t *cu_seqlens_q, int32_t total_q,
+                          const sa_kv_desc_t *kv, const int32_t *seqlens_kv, int32_t batch, int32_t num_qo_heads,
+                          int32_t max_q_len, int32_t max_kv_len, const float *sinks, int32_t window,
+                          float sm_scale, void *out, float *lse, cudaStream_t stream)
+{
+    return prefill_impl(q, true, q_scale, cu_seqlens_q, total_q, kv, seqlens_kv, batch, num_qo_heads, max_q_len,
+                        max_kv_len, sinks, window, sm_scale, out, lse, stream);
 }
 
 sa_status_t sa_rope_yarn_table(float *table, int32_t max_position, int32_t head_dim, double theta,
@@ -651,7 +684,7 @@ sa_status_t sa_rope_yarn_table(float *table, int32_t max_position, int32_t head_
 sa_status_t sa_rope_append(const void *q, const void *k, const void *v, int32_t num_tokens, int32_t num_qo_heads,
                            const int32_t *seq_ids, const int32_t *positions, const float *table,
                            int32_t max_position, const sa_kv_desc_t *kv, int32_t batch, void *q_out,
-                           cudaStream_t stream)
+                           float q_out_scale, cudaStream_t stream)
 {
     g_err[0] = 0;
     if (num_tokens < 0 || batch < 0 || max_position < 1)
@@ -659,6 +692,8 @@ sa_status_t sa_rope_append(const void *q, const void *k, const void *v, int32_t 
     sa_status_t st = check_kv(kv, batch, num_qo_heads, 0);
     if (st != SA_OK)
         return st;
+    if (!std::isfinite(q_out_scale) || q_out_scale < 0.f)
+        return fail(SA_ERR_INVALID_ARG, "q_out_scale must be 0 (bf16 q_out) or finite and > 0 (E4M3 q_out)");
     if (num_tokens == 0)
         return SA_OK;
     if (!q || !k || !v || !seq_ids || !positions || !table || !q_out)
@@ -699,6 +734,8 @@ sa_status_t sa_rope_append(const void *q, const void *k, const void *v, int32_t 
     p.fp8 = fp8 ? 1 : 0;
     p.k_inv_scale = fp8 ? 1.f / kv->k_scale : 1.f;
     p.v_inv_scale = fp8 ? 1.f / kv->v_scale : 1.f;
+    p.q_fp8 = q_out_scale > 0.f ? 1 : 0;
+    p.q_inv_scale = q_out_scale > 0.f ? 1.f / q_out_scale : 1.f;
     e = sa::launch_rope_append(p, stream);
     if (e != cudaSuccess)
         return cuda_fail(e, "rope_append launch");

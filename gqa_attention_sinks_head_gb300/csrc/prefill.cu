@@ -44,6 +44,12 @@
 // bf16 to f16 in place once, P is stored as f16, the products run as
 // kind::f16 with f16 operands, and k_scale (resp. v_scale) is folded into the
 // score scale (resp. the output scale).
+//
+// E4M3 queries on an FP8 cache (Q8; the same vLLM passage: part of the
+// attention in FP8): Q arrives as E4M3 codes and S = Q K^T runs as
+// kind::f8f6f4 straight from the TMA-staged key codes (64-byte swizzle, two
+// 32-byte K steps), so only V is widened; the MMA warp releases a staging slot
+// once the QK products that read it have completed.
 #include <cuda_bf16.h>
 
 #include "sa_internal.h"
@@ -70,6 +76,7 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 of the largest tolerated p
 // Q, K both K-major; V is MN-major (dims contiguous).  f16 operands for an FP8 cache.
 template <bool FP8>
 constexpr uint32_t kIdescQK = idesc_f32acc(BM, BN, 0, FP8);
+constexpr uint32_t kIdescQK8 = idesc_e4m3_f32acc(BM, BN);  // E4M3 Q and K
 template <bool FP8>
 constexpr uint32_t kIdescPV = idesc_f32acc(BM, kHeadDim, 1, FP8);
 
@@ -85,6 +92,7 @@ struct PrefillSmem {
     uint64_t q_full;
     uint64_t q_conv;  // FP8: Q converted to f16
     uint64_t st_full[kStaged];
+    uint64_t k8_empty[kStaged];  // Q8: the QK products that read a staging slot have completed
     uint64_t k_full[kStages];
     uint64_t v_full[kStages];
     uint64_t kv_empty[kStages];
@@ -239,12 +247,14 @@ __device__ __forceinline__ void softmax_tile(uint32_t s_addr, uint32_t o_addr, f
     }
 }
 
-template <bool FP8>
+template <bool FP8, bool Q8>
 __global__ void __launch_bounds__(kThreads, 2)
     prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                    const __grid_constant__ CUtensorMap tmv, const PrefillParams p)
 {
+    static_assert(FP8 || !Q8, "E4M3 queries need an FP8 cache");
     constexpr int kStages = PrefillSmem<FP8>::kStages;
+    constexpr uint32_t kQBytes = Q8 ? kQTileBytes / 2 : kQTileBytes;  // bytes TMA brings per Q tile
     extern __shared__ uint8_t smem_raw[];
     PrefillSmem<FP8> &sm =
         *reinterpret_cast<PrefillSmem<FP8> *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -284,8 +294,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (threadIdx.x == 0) {
         mbar_init(&sm.q_full, 1);
         mbar_init(&sm.q_conv, 4 * NH);
-        for (int i = 0; i < PrefillSmem<FP8>::kStaged; ++i)
+        for (int i = 0; i < PrefillSmem<FP8>::kStaged; ++i) {
             mbar_init(&sm.st_full[i], 1);
+            mbar_init(&sm.k8_empty[i], 1);
+        }
         for (int i = 0; i < kStages; ++i) {
             mbar_init(&sm.k_full[i], 1);
             mbar_init(&sm.v_full[i], 1);
@@ -313,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             tma_prefetch_desc(&tmq);
             tma_prefetch_desc(&tmk);
             tma_prefetch_desc(&tmv);
-            mbar_arrive_expect_tx(&sm.q_full, static_cast<uint32_t>(NH) * kQTileBytes);
+            mbar_arrive_expect_tx(&sm.q_full, static_cast<uint32_t>(NH) * kQBytes);
             for (int t = 0; t < NH; ++t)
                 tma_load_3d(sm.q[t], &tmq, &sm.q_full, 0, h0 + t, q_beg + q0);
         }
@@ -352,20 +364,27 @@ __global__ void __launch_bounds__(kThreads, 2)
             int issued = 0;
             for (int it = 0; it < ntiles; ++it) {
                 const int stage = it % kStages;
-                for (; issued < ntiles && issued < it + kStaged; ++issued)
+                for (; issued < ntiles && issued < it + kStaged; ++issued) {
+                    // Q8: the slot's previous tile must have been read by its QK products
+                    if (Q8 && issued >= kStaged &&
+                        !mbar_wait(&sm.k8_empty[issued % kStaged], ((issued / kStaged) - 1) & 1, p.status))
+                        break;
                     stage_codes(issued);
+                }
                 const int sb = it % kStaged;
                 if (!mbar_wait(&sm.st_full[sb], (it / kStaged) & 1, p.status))
                     break;
                 if (it >= kStages && !mbar_wait(&sm.kv_empty[stage], ((it / kStages) - 1) & 1, p.status))
                     break;
                 const int valid = min(BN, Lkv - (j_first + it) * BN);
-                widen_tile(sm.k8[sb], sm.k[stage], valid, lane);
+                if (!Q8)  // (Q8: the QK products read the key codes where TMA put them)
+                    widen_tile(sm.k8[sb], sm.k[stage], valid, lane);
                 widen_tile(sm.v8[sb], sm.v[stage], valid, lane);
                 fence_proxy_async_smem();  // generic writes -> tensor-core reads; staging reads -> next TMA
                 __syncwarp();
                 if (lane == 0) {
-                    mbar_arrive(&sm.k_full[stage]);
+                    if (!Q8)
+                        mbar_arrive(&sm.k_full[stage]);
                     mbar_arrive(&sm.v_full[stage]);
                 }
             }
@@ -401,16 +420,33 @@ __global__ void __launch_bounds__(kThreads, 2)
         // ============================ MMA issuer ==========================
         // Descriptor bases; a K step adds to the start-address field (bytes >> 4):
         // 32 bytes (16 dims) for Q/K, 2048 bytes (16 keys) for V.
-        const uint64_t dq0 = smem_desc_sw128(smem_u32(sm.q[0]), 16, 1024);
-        const uint64_t dk0 = smem_desc_sw128(smem_u32(sm.k[0]), 16, 1024);
+        // Q8: E4M3 Q and key codes, 64-byte rows with the 64-byte swizzle (8-row groups of 512 bytes)
+        const uint64_t dq0 = Q8 ? smem_desc(smem_u32(sm.q[0]), 16, 512, 4u) : smem_desc_sw128(smem_u32(sm.q[0]), 16, 1024);
+        const uint64_t dk0 = Q8 ? smem_desc(smem_u32(sm.k8[0]), 16, 512, 4u) : smem_desc_sw128(smem_u32(sm.k[0]), 16, 1024);
         const uint64_t dv0 = smem_desc_sw128(smem_u32(sm.v[0]), 16, 1024);
+        // stage: ring stage of K (16-bit) or staging slot of the key codes (Q8)
         auto issue_qk = [&](int t, int stage) {
             const uint64_t dq = dq0 + static_cast<uint64_t>(t) * (kQTileBytes >> 4);  // q[1] follows q[0]
-            const uint64_t dk = dk0 + static_cast<uint64_t>(stage) * (kKVTileBytes >> 4);
+            if constexpr (Q8) {
+                const uint64_t dk = dk0 + static_cast<uint64_t>(stage) * (kKV8TileBytes >> 4);
 #pragma unroll
-            for (int ks = 0; ks < kHeadDim / 16; ++ks)
-                umma_ss(tmem + col_s(t), dq + 2 * ks, dk + 2 * ks, kIdescQK<FP8>, ks > 0 ? 1u : 0u);
+                for (int ks = 0; ks < kHeadDim / 32; ++ks)  // K = 32 one-byte elements per product
+                    umma_ss_f8(tmem + col_s(t), dq + 2 * ks, dk + 2 * ks, kIdescQK8, ks > 0 ? 1u : 0u);
+            } else {
+                const uint64_t dk = dk0 + static_cast<uint64_t>(stage) * (kKVTileBytes >> 4);
+#pragma unroll
+                for (int ks = 0; ks < kHeadDim / 16; ++ks)
+                    umma_ss(tmem + col_s(t), dq + 2 * ks, dk + 2 * ks, kIdescQK<FP8>, ks > 0 ? 1u : 0u);
+            }
         };
+        constexpr int kStaged = PrefillSmem<FP8>::kStaged;
+        // K of tile j is ready: the 16-bit ring stage, or (Q8) the TMA of its staging slot
+        auto wait_k = [&](int j) -> bool {
+            if (Q8)
+                return mbar_wait(&sm.st_full[j % kStaged], (j / kStaged) & 1, p.status);
+            return mbar_wait(&sm.k_full[j % kStages], (j / kStages) & 1, p.status);
+        };
+        auto k_slot = [&](int j) { return Q8 ? j % kStaged : j % kStages; };
         auto issue_pv = [&](int t, int stage, bool accumulate) {
             const uint64_t dv = dv0 + static_cast<uint64_t>(stage) * (kKVTileBytes >> 4);
 #pragma unroll
@@ -418,14 +454,17 @@ __global__ void __launch_bounds__(kThreads, 2)
                 umma_ts(tmem + col_o(t), tmem + col_s(t) + 8 * kk, dv + 128 * kk, kIdescPV<FP8>,
                         (accumulate || kk > 0) ? 1u : 0u);
         };
-        bool ok = mbar_wait(FP8 ? &sm.q_conv : &sm.q_full, 0, p.status) && mbar_wait(&sm.k_full[0], 0, p.status);
+        bool ok = mbar_wait((FP8 && !Q8) ? &sm.q_conv : &sm.q_full, 0, p.status) && wait_k(0);
         if (ok) {
             tc_fence_after();
-            if (lane == 0)
+            if (lane == 0) {
                 for (int t = 0; t < NH; ++t) {
                     issue_qk(t, 0);
                     umma_commit(&sm.s_full[t]);
                 }
+                if (Q8)
+                    umma_commit(&sm.k8_empty[0]);
+            }
             __syncwarp();
         }
         for (int it = 0; ok && it < ntiles; ++it) {
@@ -454,21 +493,23 @@ __global__ void __launch_bounds__(kThreads, 2)
                 if (lane == 0)
                     issue_pv(t, stage, it > 0);
                 if (it + 1 < ntiles) {
-                    const int ns = (it + 1) % kStages;
-                    if (!mbar_wait(&sm.k_full[ns], ((it + 1) / kStages) & 1, p.status)) {
+                    if (!wait_k(it + 1)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     if (lane == 0) {
-                        issue_qk(t, ns);
+                        issue_qk(t, k_slot(it + 1));
                         umma_commit(&sm.s_full[t]);
                     }
                 }
                 __syncwarp();
             }
-            if (lane == 0)
+            if (lane == 0) {
                 umma_commit(&sm.kv_empty[stage]);
+                if (Q8 && ok && it + 1 < ntiles)
+                    umma_commit(&sm.k8_empty[(it + 1) % kStaged]);  // every head's QK(it + 1) is issued
+            }
             __syncwarp();
         }
         if (lane == 0)
@@ -492,7 +533,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             l = 1.f;                          // ... and the sum at 1
         }
         bool ok = true;
-        if constexpr (FP8) {
+        if constexpr (FP8 && !Q8) {
             // this thread's Q row, bf16 -> f16 in place (the swizzle only
             // permutes 16-byte chunks within the row); lanes start at
             // different chunks so that no two of 8 lanes share banks
@@ -526,7 +567,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 key0 + BN - 1 > p_first || (p.window > 0 && key0 <= p_last - p.window) || key0 + BN > Lkv;
             if (edge)
                 mask_tile(s_addr, key0, pos, Lkv, p.window);
-            softmax_tile<FP8>(s_addr, o_addr, p.score_scale, it > 0, m, l);
+            softmax_tile<FP8>(s_addr, o_addr, p.score_scale, it > 0, m, l);  // (P in f16 for both FP8 modes)
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
@@ -576,7 +617,7 @@ size_t prefill_smem_bytes()
     return sizeof(PrefillSmem<FP8>) + 1024;  // + slack for the 1 KB alignment
 }
 
-template <bool FP8>
+template <bool FP8, bool Q8>
 cudaError_t launch_of(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, const PrefillParams &p,
                       cudaStream_t stream)
 {
@@ -586,7 +627,7 @@ cudaError_t launch_of(const CUtensorMap &tq, const CUtensorMap &tk, const CUtens
     if (e != cudaSuccess)
         return e;
     if (dev < 0 || dev >= 64 || !done[dev]) {
-        e = cudaFuncSetAttribute(prefill_kernel<FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(prefill_kernel<FP8, Q8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(prefill_smem_bytes<FP8>()));
         if (e != cudaSuccess)
             return e;
@@ -594,16 +635,18 @@ cudaError_t launch_of(const CUtensorMap &tq, const CUtensorMap &tk, const CUtens
             done[dev] = 1;
     }
     const dim3 grid(p.num_qo_heads / p.heads_per_cta, p.num_q_tiles, p.batch);
-    prefill_kernel<FP8><<<grid, kThreads, prefill_smem_bytes<FP8>(), stream>>>(tq, tk, tv, p);
+    prefill_kernel<FP8, Q8><<<grid, kThreads, prefill_smem_bytes<FP8>(), stream>>>(tq, tk, tv, p);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_prefill(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                           const PrefillParams &p, bool fp8, cudaStream_t stream)
+                           const PrefillParams &p, bool fp8, bool q8, cudaStream_t stream)
 {
-    return fp8 ? launch_of<true>(tq, tk, tv, p, stream) : launch_of<false>(tq, tk, tv, p, stream);
+    if (q8)
+        return launch_of<true, true>(tq, tk, tv, p, stream);
+    return fp8 ? launch_of<true, false>(tq, tk, tv, p, stream) : launch_of<false, false>(tq, tk, tv, p, stream);
 }
 
 }  // namespace sa

@@ -78,10 +78,16 @@ __device__ __forceinline__ void finish_row(const RopeParams &p, int t, int j, in
         }
     }
     if (is_q) {
-        __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(p.q_out) +
-                             (static_cast<int64_t>(t) * p.num_qo_heads + j) * kHeadDim;
-        *reinterpret_cast<uint4 *>(dst + 8 * sub) = pack8_bf16(x1);
-        *reinterpret_cast<uint4 *>(dst + kHeadDim / 2 + 8 * sub) = pack8_bf16(x2);
+        const int64_t qoff = (static_cast<int64_t>(t) * p.num_qo_heads + j) * kHeadDim;
+        if (p.q_fp8) {
+            uint8_t *dst = reinterpret_cast<uint8_t *>(p.q_out) + qoff;
+            *reinterpret_cast<uint2 *>(dst + 8 * sub) = pack8_e4m3(x1, p.q_inv_scale);
+            *reinterpret_cast<uint2 *>(dst + kHeadDim / 2 + 8 * sub) = pack8_e4m3(x2, p.q_inv_scale);
+        } else {
+            __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(p.q_out) + qoff;
+            *reinterpret_cast<uint4 *>(dst + 8 * sub) = pack8_bf16(x1);
+            *reinterpret_cast<uint4 *>(dst + kHeadDim / 2 + 8 * sub) = pack8_bf16(x2);
+        }
         return;
     }
     // cache slot of (sequence b, position pos, kv head g)
@@ -113,7 +119,7 @@ __device__ __forceinline__ void finish_row(const RopeParams &p, int t, int j, in
 
 // Each thread takes kRowsPerThread rows, kRowsPerBlock apart, and issues all
 // their loads before the first store: more bytes in flight per thread.
-__global__ void __launch_bounds__(kThreads) rope_append_kernel(const RopeParams p)
+__global__ void __launch_bounds__(kThreads, 2) rope_append_kernel(const RopeParams p)
 {
     const int sub = threadIdx.x & 3;
     const uint32_t heads = p.num_qo_heads + 2 * p.num_kv_heads;

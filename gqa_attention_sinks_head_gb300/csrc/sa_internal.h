@@ -76,6 +76,8 @@ struct RopeParams {
     int32_t page_size, table_stride, num_pages;
     int32_t fp8;                  // cache holds E4M3 codes
     float k_inv_scale, v_inv_scale;  // FP8: 1 / k_scale, 1 / v_scale
+    int32_t q_fp8;                // q_out holds E4M3 codes of q / q_scale
+    float q_inv_scale;
 };
 
 // Record `fmt` as the calling thread's sa_last_error() message and return st.
@@ -88,6 +90,6 @@ cudaError_t decode_occupancy(bool fp8, int *blocks_per_sm);
 cudaError_t launch_merge(const MergeParams &p, cudaStream_t stream);
 cudaError_t launch_rope_append(const RopeParams &p, cudaStream_t stream);
 cudaError_t launch_prefill(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                           const PrefillParams &p, bool fp8, cudaStream_t stream);
+                           const PrefillParams &p, bool fp8, bool q8, cudaStream_t stream);
 
 }  // namespace sa

@@ -273,6 +273,23 @@ sa_status_t sa_prefill(const void *q, const int32_t *cu_seqlens_q, int32_t total
                        cudaStream_t stream);
 
 /*
+ * sa_prefill_q8 -- sa_prefill with the query given as E4M3 codes on an
+ * FP8-E4M3 cache (vLLM "GPT-OSS optimisations on NVIDIA Blackwell": part of
+ * the attention runs in FP8).  S = Q K^T runs on the FP8 tensor cores
+ * (kind::f8f6f4) straight from the cache's codes; P V as in sa_prefill.
+ *   q        device uint8 [total_q, num_qo_heads, 64]: E4M3 codes, value =
+ *            code * q_scale (sa_rope_append can write them)
+ *   q_scale  finite, nonzero
+ * Other arguments, layouts and results as sa_prefill.  SA_ERR_UNSUPPORTED
+ * for a bf16 cache.
+ */
+sa_status_t sa_prefill_q8(const void *q, float q_scale, const int32_t *cu_seqlens_q, int32_t total_q,
+                          const sa_kv_desc_t *kv, const int32_t *seqlens_kv, int32_t batch,
+                          int32_t num_qo_heads, int32_t max_q_len, int32_t max_kv_len,
+                          const float *sinks, int32_t window, float sm_scale, void *out, float *lse,
+                          cudaStream_t stream);
+
+/*
  * sa_rope_yarn_table -- fill a HOST buffer with the rotary table that
  * sa_rope_append reads: for each position p in [0, max_position), 64 floats,
  * cos(p * f_i) * mscale for i = 0..31 then sin(p * f_i) * mscale.
@@ -314,7 +331,10 @@ sa_status_t sa_rope_yarn_table(float *table, int32_t max_position, int32_t head_
  *   table        device fp32 [max_position, 64] from sa_rope_yarn_table
  *   kv           the cache to write (kv->k and kv->v are written)
  *   batch        rows of kv->page_table (sequences), or pages when it is NULL
- *   q_out        device bf16 [num_tokens, num_qo_heads, 64] (may alias q)
+ *   q_out        device [num_tokens, num_qo_heads, 64]: bf16 (q_out_scale = 0;
+ *                may alias q) or, for q_out_scale > 0, E4M3 codes of
+ *                rotate(q) / q_out_scale (round to nearest even, saturated),
+ *                the query input of sa_prefill_q8
  * A token whose sequence id or position is out of range, or whose table entry
  * lies past the table row, is skipped and sets SA_DEVICE_BAD_TOKEN; one whose
  * page is outside [0, num_pages) is skipped and sets SA_DEVICE_BAD_PAGE.
@@ -323,7 +343,7 @@ sa_status_t sa_rope_yarn_table(float *table, int32_t max_position, int32_t head_
 sa_status_t sa_rope_append(const void *q, const void *k, const void *v, int32_t num_tokens,
                            int32_t num_qo_heads, const int32_t *seq_ids, const int32_t *positions,
                            const float *table, int32_t max_position, const sa_kv_desc_t *kv,
-                           int32_t batch, void *q_out, cudaStream_t stream);
+                           int32_t batch, void *q_out, float q_out_scale, cudaStream_t stream);
 
 /*
  * sa_decode_static_workspace -- sa_decode for callers that cannot allocate

@@ -156,3 +156,14 @@ def test_decode_multi_workspace_size(lib):
     assert lib.sa_decode_multi_workspace_size(4, 3, 64, 8, 64, 1000, 0, 1) == 0
     s = lib.sa_decode_multi_workspace_size(4, 3, 64, 8, 64, 1000, 0, 5)
     assert s == lib.sa_decode_workspace_size(12, 64, 8, 64, 1000, 0, 5)  # rows = batch * q_len
+
+
+def test_prefill_q8_needs_an_fp8_cache(lib):
+    L = lib.load()
+    d = _desc(lib)  # bf16 cache
+    rc = L.sa_prefill_q8(4096, 0.1, 4096, 10, ctypes.byref(d), 4096, 2, 64, 5, 100, None, 0, 0.125, 4096, None, None)
+    assert rc == 2 and "FP8" in L.sa_last_error().decode()
+    d = _desc(lib, dtype=1)
+    rc = L.sa_prefill_q8(4096, float("nan"), 4096, 10, ctypes.byref(d), 4096, 2, 64, 5, 100, None, 0, 0.125, 4096,
+                         None, None)
+    assert rc == 1

@@ -105,3 +105,69 @@ def test_fp8_group_pairings(sa, oracle, hq, hkv):
 def test_fp8_peaked_scores_no_sinks(sa, oracle):
     case = W.make_prefill_case([300], [300], sm_scale=1.5, sinks=False, kv_dtype="e4m3", seed=312)
     run(sa, oracle, case, "fp8 scale 1.5, no sink")
+
+
+# ---- E4M3 queries on an FP8 cache (sa_prefill_q8: kind::f8f6f4 for Q K^T) ----
+def quantise_q(case):
+    """E4M3 codes of the case's q with a per-tensor scale amax / 448 (torch's
+    round-to-nearest-even cast), and that scale."""
+    q = case.q.float()
+    scale = float(q.abs().max()) / 448.0
+    codes = (q / scale).to(torch.float8_e4m3fn).view(torch.uint8)
+    return codes, scale
+
+
+def run_q8(sa, oracle, case, what, sel=None):
+    codes, q_scale = quantise_q(case)
+    g = case.to("cuda")
+    T, Hq, D = case.q.shape
+    out = torch.full((T, Hq, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((T, Hq), float("nan"), dtype=torch.float32, device="cuda")
+    cu = case.cu_seqlens_q
+    qlens = (cu[1:] - cu[:-1])
+    sa.sa_prefill_q8(codes.cuda(), q_scale, g.cu_seqlens_q, g.kv, g.seqlens, g.sinks, case.window, case.sm_scale,
+                     out, lse, max_q_len=int(qlens.max()), max_kv_len=int(case.seqlens.max()))
+    torch.cuda.synchronize()
+    assert sa.sa_device_status() == 0
+    rows = oracle.prefill_rows(case.cu_seqlens_q, case.seqlens)
+    if sel is None:
+        sel = np.arange(T, dtype=np.int32)
+    sr = np.repeat(sel, Hq)
+    sh = np.tile(np.arange(Hq, dtype=np.int32), len(sel))
+    ref_o, ref_l = oracle.attend(codes, rows[0], rows[1], case.kv.as_dict(), case.seqlens, case.sinks, case.window,
+                                 case.sm_scale, sr, sh, q_scale=q_scale)
+    check_close(out[sel], lse[sel], ref_o.reshape(len(sel), Hq, D), ref_l.reshape(len(sel), Hq), what)
+
+
+@pytest.mark.parametrize("T", [1, 63, 129, 700])
+@pytest.mark.parametrize("window", [0, 128])
+def test_q8_single_sequence(sa, oracle, T, window):
+    case = W.make_prefill_case([T], [T], window=window, kv_dtype="e4m3", seed=320 + T)
+    run_q8(sa, oracle, case, "q8 T=%d w=%d" % (T, window))
+
+
+@pytest.mark.parametrize("layout", ["HND", "NHD"])
+@pytest.mark.parametrize("window", [0, 128])
+def test_q8_paged_ragged(sa, oracle, layout, window):
+    case = W.make_prefill_case([200, 77, 5, 130], [520, 77, 1000, 131], paged=True, page_size=16, layout=layout,
+                               window=window, kv_dtype="e4m3", poison_pages=5, seed=330)
+    run_q8(sa, oracle, case, "q8 paged %s w=%d" % (layout, window))
+
+
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (6, 2)])
+def test_q8_group_pairings(sa, oracle, hq, hkv):
+    case = W.make_prefill_case([150], [150], num_qo_heads=hq, num_kv_heads=hkv, kv_dtype="e4m3", seed=331)
+    run_q8(sa, oracle, case, "q8 Hq=%d Hkv=%d" % (hq, hkv))
+
+
+def test_q8_peaked_scores_no_sinks(sa, oracle):
+    case = W.make_prefill_case([300], [300], sm_scale=1.5, sinks=False, kv_dtype="e4m3", seed=332)
+    run_q8(sa, oracle, case, "q8 scale 1.5, no sink")
+
+
+def test_q8_config7_full_size(sa, oracle):
+    case = W.make_config(7, window=0)
+    g = np.random.default_rng(97)
+    sel = np.unique(np.concatenate([np.arange(0, 8192, 1024), np.arange(1023, 8192, 1024),
+                                    g.choice(8192, 40, replace=False)])).astype(np.int32)
+    run_q8(sa, oracle, case, "q8 config 7", sel=sel)

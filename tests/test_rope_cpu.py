@@ -53,7 +53,7 @@ def test_append_argument_checks(sa):
     d.page_table, d.k_scale, d.v_scale = 1024, 1.0, 1.0
     args = lambda **kw: [kw.get("q", 4096), 4096, 4096, kw.get("T", 3), kw.get("hq", 64), 4096, 4096,
                          kw.get("table", 4096), kw.get("maxpos", 100), ctypes.byref(d), kw.get("batch", 2),
-                         kw.get("qo", 4096), None]
+                         kw.get("qo", 4096), kw.get("qs", 0.0), None]
     assert L.sa_rope_append(*args(T=0)) == 0
     assert L.sa_rope_append(*args(T=-1)) == 1
     assert L.sa_rope_append(*args(maxpos=0)) == 1
@@ -61,3 +61,5 @@ def test_append_argument_checks(sa):
     assert L.sa_rope_append(*args(q=None)) == 1
     assert L.sa_rope_append(*args(q=4100)) == 2
     assert L.sa_rope_append(*args(table=4104)) == 2
+    assert L.sa_rope_append(*args(qs=-1.0)) == 1
+    assert L.sa_rope_append(*args(qs=float("inf"))) == 1

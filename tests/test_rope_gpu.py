@@ -143,3 +143,29 @@ def test_bad_tokens_are_skipped_and_flagged(sa):
     assert r["flags"] & SA_DEVICE_BAD_TOKEN
     check(r)
     assert_untouched(r)
+
+
+def test_fp8_query_output(sa):
+    """q_out as E4M3 codes of rotate(q) / q_out_scale: the oracle's encoder
+    on the fp64 rotation, up to a neighbouring code at rounding midpoints."""
+    seqlens, new = [300, 40], [300, 40]
+    kv = W.make_kv(seqlens, 8, 64, 16, paged=True, kv_dtype="e4m3", seed=505, layout="HND")
+    seq, pos, g = _tokens(seqlens, new, 505)
+    T = len(seq)
+    q = torch.from_numpy(g.standard_normal((T, 64, 64)).astype(np.float32)).to(torch.bfloat16)
+    k = torch.from_numpy(g.standard_normal((T, 8, 64)).astype(np.float32)).to(torch.bfloat16)
+    v = torch.from_numpy(g.standard_normal((T, 8, 64)).astype(np.float32)).to(torch.bfloat16)
+    table = sa.sa_rope_yarn_table(512, **YARN)
+    q_scale = 0.02
+    q_codes = torch.zeros(T, 64, 64, dtype=torch.uint8, device="cuda")
+    sa.sa_rope_append(q.cuda(), k.cuda(), v.cuda(), torch.from_numpy(seq).cuda(), torch.from_numpy(pos).cuda(),
+                      table.cuda(), kv.to("cuda"), 2, q_codes, q_out_scale=q_scale)
+    torch.cuda.synchronize()
+    assert sa.sa_device_status() == 0
+    f, ms = R.yarn_inv_freq(64, **YARN)
+    want = R.e4m3_encode(R.rope_rotate(q.double().numpy(), pos[:, None], f, ms) / q_scale)
+    got = q_codes.cpu().numpy()
+    mism = got != want
+    a, b = got[mism].astype(np.int64), want[mism].astype(np.int64)
+    assert np.all((a & 0x80) == (b & 0x80)) and np.all(np.abs((a & 0x7F) - (b & 0x7F)) == 1)
+    assert mism.sum() <= 4, int(mism.sum())
