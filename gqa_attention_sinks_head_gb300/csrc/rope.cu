@@ -10,7 +10,7 @@
 // is read once and written once.  Four threads share a row: thread s handles
 // dims 8s..8s+7 of the first half and the same dims of the second half, the
 // pairs the rotation mixes, with 16-byte loads and stores; each thread takes
-// four rows and loads all of them before it stores any.  cos and sin come
+// three rows and loads all of them before it stores any.  cos and sin come
 // from a table the host fills in double precision (sa_rope_yarn_table), so no
 // large-angle argument reduction runs in fp32 on the device.
 #include <cuda_bf16.h>
@@ -22,7 +22,7 @@ namespace sa {
 namespace {
 
 constexpr int kRowsPerBlock = 64;  // rows one pass of the block covers (4 threads per row)
-constexpr int kRowsPerThread = 4;
+constexpr int kRowsPerThread = 3;
 constexpr int kThreads = 4 * kRowsPerBlock;
 
 __device__ __forceinline__ void unpack8(const uint4 &w, float (&f)[8])
@@ -58,6 +58,7 @@ __device__ __forceinline__ uint2 pack8_e4m3(const float (&f)[8], float inv_scale
 
 // One head row: rotate (unless it is v) and store.  x1/x2 hold dims 8s..8s+7
 // of the two halves.
+template <bool kCacheFp8, bool kQFp8>
 __device__ __forceinline__ void finish_row(const RopeParams &p, int t, int j, int pos, int b, int sub, float (&x1)[8],
                                            float (&x2)[8])
 {
@@ -79,7 +80,7 @@ __device__ __forceinline__ void finish_row(const RopeParams &p, int t, int j, in
     }
     if (is_q) {
         const int64_t qoff = (static_cast<int64_t>(t) * p.num_qo_heads + j) * kHeadDim;
-        if (p.q_fp8) {
+        if (kQFp8) {
             uint8_t *dst = reinterpret_cast<uint8_t *>(p.q_out) + qoff;
             *reinterpret_cast<uint2 *>(dst + 8 * sub) = pack8_e4m3(x1, p.q_inv_scale);
             *reinterpret_cast<uint2 *>(dst + kHeadDim / 2 + 8 * sub) = pack8_e4m3(x2, p.q_inv_scale);
@@ -105,7 +106,7 @@ __device__ __forceinline__ void finish_row(const RopeParams &p, int t, int j, in
     }
     const int64_t off = static_cast<int64_t>(page) * p.stride_page + static_cast<int64_t>(g) * p.stride_head +
                         static_cast<int64_t>(pos % p.page_size) * p.stride_token;
-    if (p.fp8) {
+    if (kCacheFp8) {
         uint8_t *dst = reinterpret_cast<uint8_t *>(is_v ? p.v_cache : p.k_cache) + off;
         const float inv = is_v ? p.v_inv_scale : p.k_inv_scale;
         *reinterpret_cast<uint2 *>(dst + 8 * sub) = pack8_e4m3(x1, inv);
@@ -119,7 +120,8 @@ __device__ __forceinline__ void finish_row(const RopeParams &p, int t, int j, in
 
 // Each thread takes kRowsPerThread rows, kRowsPerBlock apart, and issues all
 // their loads before the first store: more bytes in flight per thread.
-__global__ void __launch_bounds__(kThreads, 2) rope_append_kernel(const RopeParams p)
+template <bool kCacheFp8, bool kQFp8>
+__global__ void __launch_bounds__(kThreads, 3) rope_append_kernel(const RopeParams p)
 {
     const int sub = threadIdx.x & 3;
     const uint32_t heads = p.num_qo_heads + 2 * p.num_kv_heads;
@@ -162,7 +164,7 @@ __global__ void __launch_bounds__(kThreads, 2) rope_append_kernel(const RopePara
         float x1[8], x2[8];
         unpack8(w1[r], x1);
         unpack8(w2[r], x2);
-        finish_row(p, tt[r], jj[r], pp[r], bb[r], sub, x1, x2);
+        finish_row<kCacheFp8, kQFp8>(p, tt[r], jj[r], pp[r], bb[r], sub, x1, x2);
     }
 }
 
@@ -175,7 +177,13 @@ cudaError_t launch_rope_append(const RopeParams &p, cudaStream_t stream)
     const int64_t blocks = (rows + per_block - 1) / per_block;
     if (blocks == 0)
         return cudaSuccess;
-    rope_append_kernel<<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(p);
+    const unsigned nb = static_cast<unsigned>(blocks);
+    if (p.fp8)
+        p.q_fp8 ? rope_append_kernel<true, true><<<nb, kThreads, 0, stream>>>(p)
+                : rope_append_kernel<true, false><<<nb, kThreads, 0, stream>>>(p);
+    else
+        p.q_fp8 ? rope_append_kernel<false, true><<<nb, kThreads, 0, stream>>>(p)
+                : rope_append_kernel<false, false><<<nb, kThreads, 0, stream>>>(p);
     return cudaGetLastError();
 }
 
