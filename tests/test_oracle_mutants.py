@@ -2,6 +2,7 @@
 
 Each case plants one mistake in a copy of oracle/sa_oracle.c (on the CPU),
 builds it, and runs the pin suite against that build: the suite must fail.
+The same for the rotary oracle, oracle/rope.py, against its own pins.
 """
 import os
 import subprocess
@@ -50,5 +51,36 @@ def test_pins_catch_planted_mistake(name, tmp_path):
     env = dict(os.environ, SA_ORACLE_LIB=str(lib))
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                         os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode != 0, "pins did not notice: " + name
+
+
+ROPE_SRC = os.path.join(ROOT, "oracle", "rope.py")
+ROPE_MUTANTS = {
+    "rotation pairs neighbouring dims":
+        ("    x1, x2 = x[..., :half], x[..., half:]\n    return np.concatenate([x1 * c - x2 * s, x2 * c + x1 * s], axis=-1)",
+         "    x1, x2 = x[..., 0::2], x[..., 1::2]\n    y = np.empty_like(x)\n    y[..., 0::2] = x1 * c - x2 * s\n"
+         "    y[..., 1::2] = x2 * c + x1 * s\n    return y"),
+    "rotation sign": ("x2 * c + x1 * s], axis=-1)", "x2 * c - x1 * s], axis=-1)"),
+    "frequency exponent": ("base = theta ** (-2.0 * i / d)", "base = theta ** (-1.0 * i / d)"),
+    "ramp direction": ("freq = base * (1.0 - g) + (base / factor) * g", "freq = base * g + (base / factor) * (1.0 - g)"),
+    "no attention temperature": ("mscale = 0.1 * math.log(factor) + 1.0", "mscale = 1.0"),
+    "beta roles swapped": ("lo = max(math.floor(turns_dim(beta_fast)), 0)", "lo = max(math.floor(turns_dim(beta_slow)), 0)"),
+    "E4M3 ties away from zero": ("    if r > 0.5 or (r == 0.5 and f % 2 == 1):", "    if r >= 0.5:"),
+    "E4M3 saturates to the NaN code": ("o[n] = sign | 0x7E", "o[n] = sign | 0x7F"),
+    "cache slot ignores the page size": ("(p % P) * cache[\"stride_token\"]", "(p % 16) * cache[\"stride_token\"]"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(ROPE_MUTANTS))
+def test_rope_pins_catch_planted_mistake(name, tmp_path):
+    old, new = ROPE_MUTANTS[name]
+    src = open(ROPE_SRC).read()
+    assert src.count(old) >= 1, "mutation site not found: " + name
+    mutated = tmp_path / "rope_mutant.py"
+    mutated.write_text(src.replace(old, new))
+    env = dict(os.environ, SA_ROPE_ORACLE=str(mutated))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_rope_oracle_pins.py")],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, "pins did not notice: " + name
