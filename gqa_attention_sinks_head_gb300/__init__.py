@@ -17,7 +17,7 @@ __all__ = [
     "SinkAttnError", "KVDesc", "load", "build", "sa_decode", "sa_decode_partial", "sa_merge_states",
     "sa_prefill", "sa_decode_static_workspace", "sa_decode_num_splits", "sa_decode_workspace_size", "sa_device_status", "sa_version",
     "sa_decode_multi", "sa_decode_multi_workspace_size", "SA_MAX_DECODE_TOKENS", "sa_rope_yarn_table",
-    "sa_rope_append", "sa_prefill_q8",
+    "sa_rope_append", "sa_prefill_q8", "sa_selftest_wait_timeout",
     "SA_KV_BF16", "SA_KV_FP8_E4M3", "kv_desc",
 ]
 
@@ -31,7 +31,7 @@ SA_DEVICE_SEQLEN_RANGE, SA_DEVICE_BAD_PAGE, SA_DEVICE_TIMEOUT, SA_DEVICE_BAD_QLE
 EXPORTS = ["sa_decode", "sa_decode_num_splits", "sa_decode_workspace_size", "sa_decode_partial",
            "sa_merge_states", "sa_prefill", "sa_device_status", "sa_status_string", "sa_last_error",
            "sa_version", "sa_decode_static_workspace", "sa_decode_multi", "sa_decode_multi_workspace_size",
-           "sa_rope_yarn_table", "sa_rope_append", "sa_prefill_q8"]
+           "sa_rope_yarn_table", "sa_rope_append", "sa_prefill_q8", "sa_selftest_wait_timeout"]
 SA_MAX_DECODE_TOKENS = 8
 SA_STATIC_WORKSPACE_BYTES = 16 << 20
 
@@ -85,6 +85,7 @@ def load(path: str | None = None):
     lib.sa_rope_yarn_table.argtypes = [P, i32, i32, dbl, dbl, i32, dbl, dbl]
     lib.sa_rope_append.argtypes = [P, P, P, i32, i32, P, P, P, i32, KP, i32, P, f32, P]
     lib.sa_prefill_q8.argtypes = [P, f32, P, i32, KP, P, i32, i32, i32, i32, P, i32, f32, P, P, P]
+    lib.sa_selftest_wait_timeout.argtypes = [P]
     lib.sa_decode_partial.argtypes = [P, KP, P, i32, i32, i32, i32, f32, i32, P, P, P]
     lib.sa_merge_states.argtypes = [P, P, i32, i32, i32, i32, P, P, P, P]
     lib.sa_prefill.argtypes = [P, P, i32, KP, P, i32, i32, i32, i32, P, i32, f32, P, P, P]
@@ -98,7 +99,8 @@ def load(path: str | None = None):
     lib.sa_last_error.restype = ctypes.c_char_p
     lib.sa_version.restype = ctypes.c_int
     for fn in ("sa_decode", "sa_decode_static_workspace", "sa_decode_partial", "sa_merge_states", "sa_prefill",
-               "sa_device_status", "sa_decode_multi", "sa_rope_yarn_table", "sa_rope_append", "sa_prefill_q8"):
+               "sa_device_status", "sa_decode_multi", "sa_rope_yarn_table", "sa_rope_append", "sa_prefill_q8",
+               "sa_selftest_wait_timeout"):
         getattr(lib, fn).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -268,6 +270,12 @@ def sa_prefill_q8(q_codes, q_scale, cu_seqlens_q, kv, seqlens_kv, sinks, window,
                              ctypes.byref(desc), _ptr(seqlens_kv), B, Hq, int(max_q_len), int(max_kv_len),
                              _ptr(sinks), int(window), float(sm_scale), _ptr(out), _ptr(lse), _stream(stream)))
     return out, lse
+
+
+def sa_selftest_wait_timeout(stream=None):
+    """Queue the bounded-wait self-test (about 1 s on the device); read the
+    result with sa_device_status()."""
+    _check(load().sa_selftest_wait_timeout(_stream(stream)))
 
 
 def sa_device_status(stream=None) -> int:

@@ -742,6 +742,19 @@ sa_status_t sa_rope_append(const void *q, const void *k, const void *v, int32_t 
     return SA_OK;
 }
 
+sa_status_t sa_selftest_wait_timeout(cudaStream_t stream)
+{
+    g_err[0] = 0;
+    uint32_t *status = nullptr;
+    cudaError_t e = status_ptr(&status);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "device status word");
+    e = sa::launch_wait_timeout_selftest(status, stream);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "self-test launch");
+    return SA_OK;
+}
+
 sa_status_t sa_device_status(cudaStream_t stream, uint32_t *flags_out)
 {
     uint32_t *dptr = nullptr;

@@ -89,6 +89,7 @@ cudaError_t launch_decode(const CUtensorMap &tk, const CUtensorMap &tv, const De
 cudaError_t decode_occupancy(bool fp8, int *blocks_per_sm);
 cudaError_t launch_merge(const MergeParams &p, cudaStream_t stream);
 cudaError_t launch_rope_append(const RopeParams &p, cudaStream_t stream);
+cudaError_t launch_wait_timeout_selftest(uint32_t *status, cudaStream_t stream);
 cudaError_t launch_prefill(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                            const PrefillParams &p, bool fp8, bool q8, cudaStream_t stream);
 

@@ -378,6 +378,16 @@ sa_status_t sa_decode_static_workspace(const void *q, const sa_kv_desc_t *kv, co
                                        float *lse, int32_t num_splits, cudaStream_t stream);
 
 /*
+ * sa_selftest_wait_timeout -- exercise the failure path of the pipeline waits
+ * on the device: two blocks wait on a shared-memory barrier that nothing
+ * completes, through the same bounded wait as every kernel of the library
+ * (about 1 s), then set SA_DEVICE_TIMEOUT and return.  The context stays
+ * usable.  For failure-detection tests; queues work on `stream` and returns.
+ * Returns SA_OK or SA_ERR_CUDA.
+ */
+sa_status_t sa_selftest_wait_timeout(cudaStream_t stream);
+
+/*
  * sa_device_status -- synchronise `stream`, then read and clear the device
  * status word (SA_DEVICE_* bits) of the current device.  The only call that
  * blocks the host.  Returns SA_OK or SA_ERR_CUDA.
