@@ -171,6 +171,28 @@ def dist_max(value: float, world: int) -> float:
     return float(t.item())
 
 
+L2_FLUSH_BYTES = 256 << 20  # about twice the GB300's 129 MB L2
+
+
+def timed_loop(torch, stream, one, steps, warmup, flush=None):
+    """Mean device time (ms) of one() over `steps` iterations after `warmup`,
+    each bracketed by CUDA events on `stream`; flush() (if any) runs before
+    each iteration, outside its events."""
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            one()
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for e0, e1 in evs:
+            if flush is not None:
+                flush()
+            e0.record(stream)
+            one()
+            e1.record(stream)
+        torch.cuda.synchronize()
+    return sum(e0.elapsed_time(e1) for e0, e1 in evs) / steps
+
+
 # --------------------------------------------------------------- workloads
 def decode_bytes(seqlens, window, hkv, hq, dim, elem_bytes, with_lse=True):
     """Algorithmic HBM bytes of one decode call: every visible K and V element
@@ -264,6 +286,10 @@ class DecodeBench:
     def amount(self):
         return self.step_bytes / 1e9
 
+    def resident_bytes(self):
+        """Bytes of the step's inputs in HBM: the cache the largest call reads."""
+        return max(cl["bytes"] for cl in self.calls)
+
     def run_call(self, cl, stream, ev=None):
         """Per call: [ev0] decode kernel [ev1] merge kernel.  For S > 1 this is
         sa_decode_partial + sa_merge_states, the two launches sa_decode makes."""
@@ -289,8 +315,25 @@ class DecodeBench:
     def dominant(self):
         return 0, "decode_kernel", self.calls[0]["bytes"]
 
+    def segments(self, stream):
+        """The step as launch segments: decode kernel, then its merge when split."""
+        sa, c = self.sa, self.case
+        segs = []
+        for cl in self.calls:
+            if cl["S"] > 1:
+                segs.append(lambda cl=cl: sa.sa_decode_partial(c.q, c.kv, c.seqlens, cl["window"], c.sm_scale, cl["S"],
+                                                               cl["o_part"], cl["l_part"], max_kv_len=self.maxlen,
+                                                               stream=stream))
+                segs.append(lambda cl=cl: sa.sa_merge_states(cl["o_part"], cl["l_part"], c.sinks, cl["out"],
+                                                             cl["lse"], stream=stream))
+            else:
+                segs.append(lambda cl=cl: sa.sa_decode(c.q, c.kv, c.seqlens, c.sinks, cl["window"], c.sm_scale,
+                                                       cl["out"], cl["lse"], max_kv_len=self.maxlen, num_splits=1,
+                                                       stream=stream))
+        return segs
+
     # ---- end to end through sa_decode with host buffers
-    def e2e(self, stream, steps, warmup):
+    def e2e(self, stream, steps, warmup, flush=None):
         torch = self.torch
         c = self.case
         hq = torch.empty(c.q.shape, dtype=c.q.dtype, pin_memory=True).copy_(c.q.cpu())
@@ -314,17 +357,7 @@ class DecodeBench:
                 ho.copy_(cl["out"], non_blocking=True)
                 hl.copy_(cl["lse"], non_blocking=True)
 
-        with torch.cuda.stream(stream):
-            for _ in range(warmup):
-                one()
-            torch.cuda.synchronize()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for _ in range(steps):
-                one()
-            e1.record(stream)
-            torch.cuda.synchronize()
-        ms = e0.elapsed_time(e1) / steps
+        ms = timed_loop(torch, stream, one, steps, warmup, flush)
         return ms, h2d, d2h
 
     # ---- oracle on a bounded sample
@@ -389,6 +422,9 @@ class MultiDecodeBench:
     def amount(self):
         return self.step_bytes / 1e9
 
+    def resident_bytes(self):
+        return max(cl["bytes"] for cl in self.calls)
+
     def run_call(self, cl, stream, ev=None):
         c = self.case
         if ev is not None:
@@ -406,7 +442,11 @@ class MultiDecodeBench:
     def dominant(self):
         return 0, "decode_kernel (with its merge)", self.calls[0]["bytes"]
 
-    def e2e(self, stream, steps, warmup):
+    def segments(self, stream):
+        """The step as launch segments: one per call."""
+        return [lambda cl=cl: self.run_call(cl, stream) for cl in self.calls]
+
+    def e2e(self, stream, steps, warmup, flush=None):
         torch = self.torch
         c = self.case
         hq = torch.empty(c.q.shape, dtype=c.q.dtype, pin_memory=True).copy_(c.q.cpu())
@@ -426,17 +466,8 @@ class MultiDecodeBench:
                 ho.copy_(cl["out"], non_blocking=True)
                 hl.copy_(cl["lse"], non_blocking=True)
 
-        with torch.cuda.stream(stream):
-            for _ in range(warmup):
-                one()
-            torch.cuda.synchronize()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for _ in range(steps):
-                one()
-            e1.record(stream)
-            torch.cuda.synchronize()
-        return e0.elapsed_time(e1) / steps, h2d, d2h
+        ms = timed_loop(torch, stream, one, steps, warmup, flush)
+        return ms, h2d, d2h
 
     def oracle_sample(self, budget_s, max_seqs=None):
         """Every token row of the first n sequences, all heads, every call."""
@@ -500,6 +531,9 @@ class RopeBench:
     def amount(self):
         return self.step_bytes / 1e9
 
+    def resident_bytes(self):
+        return sum(t.numel() * t.element_size() for t in (self.q, self.k, self.v))
+
     def run_call(self, cl, stream, ev=None):
         if ev is not None:
             ev[0].record(stream)
@@ -514,7 +548,11 @@ class RopeBench:
     def dominant(self):
         return 0, "rope_append_kernel", self.step_bytes
 
-    def e2e(self, stream, steps, warmup):
+    def segments(self, stream):
+        """The step as launch segments: one per call."""
+        return [lambda cl=cl: self.run_call(cl, stream) for cl in self.calls]
+
+    def e2e(self, stream, steps, warmup, flush=None):
         torch = self.torch
         hs = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t.cpu()) for t in
               (self.q, self.k, self.v, self.pos)]
@@ -528,17 +566,8 @@ class RopeBench:
             self.run_call(self.calls[0], stream)
             hout.copy_(self.q_out, non_blocking=True)
 
-        with torch.cuda.stream(stream):
-            for _ in range(warmup):
-                one()
-            torch.cuda.synchronize()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for _ in range(steps):
-                one()
-            e1.record(stream)
-            torch.cuda.synchronize()
-        return e0.elapsed_time(e1) / steps, h2d, d2h
+        ms = timed_loop(torch, stream, one, steps, warmup, flush)
+        return ms, h2d, d2h
 
     def oracle_sample(self, budget_s, max_seqs=None):
         """The oracle's rotation + cache write of the first n tokens."""
@@ -612,6 +641,12 @@ class PrefillBench:
     def amount(self):
         return self.step_flops / 1e12
 
+    def resident_bytes(self):
+        """q (or its codes) and the cache."""
+        c = self.case
+        q = self.q_codes if self.q8 else c.q
+        return q.numel() * q.element_size() + (c.kv.k.numel() + c.kv.v.numel()) * c.kv.k.element_size()
+
     def run_call(self, cl, stream, ev=None):
         c = self.case
         if ev is not None:
@@ -633,7 +668,11 @@ class PrefillBench:
     def dominant(self):
         return 0, "prefill_kernel", self.calls[0]["flops"]
 
-    def e2e(self, stream, steps, warmup):
+    def segments(self, stream):
+        """The step as launch segments: one per call."""
+        return [lambda cl=cl: self.run_call(cl, stream) for cl in self.calls]
+
+    def e2e(self, stream, steps, warmup, flush=None):
         torch = self.torch
         c = self.case
         qdev = self.q_codes if self.q8 else c.q
@@ -654,17 +693,8 @@ class PrefillBench:
                 ho.copy_(cl["out"], non_blocking=True)
                 hl.copy_(cl["lse"], non_blocking=True)
 
-        with torch.cuda.stream(stream):
-            for _ in range(warmup):
-                one()
-            torch.cuda.synchronize()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for _ in range(steps):
-                one()
-            e1.record(stream)
-            torch.cuda.synchronize()
-        return e0.elapsed_time(e1) / steps, h2d, d2h
+        ms = timed_loop(torch, stream, one, steps, warmup, flush)
+        return ms, h2d, d2h
 
     def oracle_sample(self, budget_s, max_seqs=None):
         """Rows of the sequence, all heads: the first, then every k-th."""
@@ -712,26 +742,48 @@ def run_native(args, world, rank, local):
         for _ in range(args.warmup):
             wl.step(stream)
     torch.cuda.synchronize()
-    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in wl.calls] for _ in range(steps)]
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
+    # Inputs smaller than twice the L2 (129 MB) are evicted before every step
+    # by a 256 MB write outside the step's events.
+    flush_buf = None
+    if wl.resident_bytes() < L2_FLUSH_BYTES:
+        flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    ci, kname, kbytes = wl.dominant()
+    # The step is a short list of launch segments (a kernel, or a call); events
+    # between the segments time the step and its dominant kernel on the
+    # launching stream.  --graph captures each segment once as a CUDA graph
+    # and replays it (measured: no faster here, since the L2 flush before each
+    # step leaves the host ahead of the device, and it drops the programmatic
+    # launch overlap of the decode merge).
+    segs = wl.segments(stream)
+    runs = list(segs)
+    if args.graph:
+        runs = []
+        for fn in segs:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                fn()
+            runs.append(g.replay)
+        torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(runs) + 1)] for _ in range(steps)]
     dist_barrier(world)
     torch.cuda.synchronize()
     if sampler:
         sampler.begin()
     with torch.cuda.stream(stream):
-        t_start.record(stream)
         for i in range(steps):
-            wl.step(stream, evs[i])
-        t_end.record(stream)
+            if flush_buf is not None:
+                flush_buf.zero_()
+            evs[i][0].record(stream)
+            for j, run in enumerate(runs):
+                run()
+                evs[i][j + 1].record(stream)
     torch.cuda.synchronize()
     if sampler:
         sampler.end()
     dist_barrier(world)
-    ms = t_start.elapsed_time(t_end) / steps
+    ms = statistics.fmean(e[0].elapsed_time(e[-1]) for e in evs)
     ms = dist_max(ms, world)
-    ci, kname, kbytes = wl.dominant()
-    k_ms = statistics.fmean(evs[i][ci][0].elapsed_time(evs[i][ci][1]) for i in range(steps))
+    k_ms = statistics.fmean(e[ci].elapsed_time(e[ci + 1]) for e in evs)
     clocks = sampler.stop() if sampler else None
 
     peaks, peak_src = load_peaks()
@@ -747,7 +799,8 @@ def run_native(args, world, rank, local):
         bound, nominal = "tensor", 2250.0
     traffic = ncu_traffic(kname, "config%d" % cfg)
 
-    e2e_ms, h2d, d2h = wl.e2e(stream, max(3, min(steps, 200)), 3)
+    e2e_ms, h2d, d2h = wl.e2e(stream, max(3, min(steps, 200)), 3,
+                              None if flush_buf is None else flush_buf.zero_)
     e2e_value = wl.amount() * world / (e2e_ms / 1e3)
 
     line = {
@@ -758,8 +811,12 @@ def run_native(args, world, rank, local):
         "config": {"workload": workload_name(cfg), "global_batch": wl.B * world, "seq_len_max": wl.maxlen,
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "splits": [cl.get("S", 1) for cl in wl.calls],
-                   "l2": ("inputs larger than L2 (%.2f GB of KV per step); no flush" % (wl.step_bytes / 1e9))
-                   if wl.unit == "GB/s" else "compute-bound; no flush"},
+                   "l2": ("flushed before every step (256 MB write, outside the step's events)"
+                          if flush_buf is not None else
+                          "inputs larger than twice the L2 (%.2f GB per step); no flush" % (wl.resident_bytes() / 1e9)),
+                   "launch": "each launch segment of the step captured as a CUDA graph and replayed"
+                             if args.graph else "eager",
+                   "timing": "CUDA events around each step on its stream; mean over the steps"},
         "roofline": {"bound": bound, "achieved": round(achieved, 1), "peak": peak, "unit": wl.unit,
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "kernel": kname, ("algorithmic_bytes_per_launch" if bound == "hbm"
@@ -769,7 +826,7 @@ def run_native(args, world, rank, local):
         "clocks": clocks,
         "e2e": {"value": round(e2e_value, 2), "unit": wl.unit, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "api": wl.e2e_api},
-        "gpu_launches": steps * wl.kernels_per_step,
+        "gpu_launches": steps * wl.kernels_per_step,  # the library's kernels (the L2 flush is torch's)
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
@@ -849,6 +906,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5, 6, 7, 8, 9, 10])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--graph", action="store_true",
+                    help="capture each launch segment of the step as a CUDA graph and replay it")
     ap.add_argument("--budget-s", type=float, default=120.0,
                     help="reference arm: host seconds the whole --steps/--warmup run may take")
     args = ap.parse_args(argv)
