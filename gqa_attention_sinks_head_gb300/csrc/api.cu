@@ -327,8 +327,8 @@ sa_status_t launch_decode_kernel(const void *q, int32_t q_len, const sa_kv_desc_
     p.dim_token = dt;
     p.dim_head = dh;
     p.dim_page = dp;
-    p.score_scale = sm_scale * kLog2e * (fp8 ? kv->k_scale * 256.f : 1.f);
-    p.out_scale = fp8 ? kv->v_scale * 256.f : 1.f;
+    p.score_scale = sm_scale * kLog2e * (fp8 ? kv->k_scale : 1.f);  // FP8: codes widen to their values
+    p.out_scale = fp8 ? kv->v_scale : 1.f;
     e = sa::launch_decode(tk, tv, p, fp8, stream);
     if (e != cudaSuccess)
         return cuda_fail(e, "decode launch");

@@ -28,10 +28,10 @@
 // sink-free partial state for sa_merge_states.
 //
 // FP8-E4M3 caches (vLLM "GPT-OSS optimisations on NVIDIA Blackwell", FP8 KV
-// cache) are widened in registers to f16 holding code * 2^-8 (exact for every
-// code, see e4m3x2_to_f16x2_scaled), the products run as f16 mma, and
-// 2^8 * k_scale (resp. 2^8 * v_scale) is folded into the score scale (resp.
-// the output scale).  Q is rounded to f16 for that path.
+// cache) are widened in registers to f16 (cvt e4m3x2 -> f16x2, exact for
+// every code), the products run as f16 mma, and k_scale (resp. v_scale) is
+// folded into the score scale (resp. the output scale).  Q is rounded to f16
+// for that path.
 //
 // Multi-token decode (q_len 2..8 new tokens per sequence, as a speculative or
 // multi-token-prediction verifier sends them; "GPT-OSS on day 0", the engine's
@@ -284,11 +284,11 @@ __global__ void __launch_bounds__(kThreads, TPW == 1 ? 4 : 3) decode_kernel(cons
                         for (int j2 = 0; j2 < 2; ++j2) {
                             uint32_t R0, R1, R2, R3;
                             ldsm_x4(kt + swz<true>((mi & 1) * 8 + lr, 2 * j2 + (mi >> 1)), R0, R1, R2, R3);
-                            mma_f16(s, e4m3x2_to_f16x2_scaled<kSel01>(R0), e4m3x2_to_f16x2_scaled<kSel01>(R1),
-                                    e4m3x2_to_f16x2_scaled<kSel23>(R0), e4m3x2_to_f16x2_scaled<kSel23>(R1),
+                            mma_f16(s, e4m3x2_to_f16x2(R0), e4m3x2_to_f16x2(R1), e4m3x2_to_f16x2(R0 >> 16),
+                                    e4m3x2_to_f16x2(R1 >> 16),
                                     qf[tt][2 * j2][0], qf[tt][2 * j2][1]);
-                            mma_f16(s, e4m3x2_to_f16x2_scaled<kSel01>(R2), e4m3x2_to_f16x2_scaled<kSel01>(R3),
-                                    e4m3x2_to_f16x2_scaled<kSel23>(R2), e4m3x2_to_f16x2_scaled<kSel23>(R3),
+                            mma_f16(s, e4m3x2_to_f16x2(R2), e4m3x2_to_f16x2(R3), e4m3x2_to_f16x2(R2 >> 16),
+                                    e4m3x2_to_f16x2(R3 >> 16),
                                     qf[tt][2 * j2 + 1][0], qf[tt][2 * j2 + 1][1]);
                         }
                     } else {
@@ -378,12 +378,13 @@ __global__ void __launch_bounds__(kThreads, TPW == 1 ? 4 : 3) decode_kernel(cons
                             uint32_t R0, R1, R2, R3;
                             ldsm_x4_t(vt + swz<true>((mi & 1) * 8 + lr, 2 * j2 + (mi >> 1)), R0, R1, R2, R3);
                             // rows of m-tile 2*j2 (+1): row r <-> dim 16ch + 2r, row r+8 <-> 16ch + 2r + 1
-                            mma_f16(oo[2 * j2], e4m3x2_to_f16x2_scaled<kSel02>(R0) & vm01,
-                                    e4m3x2_to_f16x2_scaled<kSel13>(R0) & vm01, e4m3x2_to_f16x2_scaled<kSel02>(R1) & vm23,
-                                    e4m3x2_to_f16x2_scaled<kSel13>(R1) & vm23, pb0, pb1);
-                            mma_f16(oo[2 * j2 + 1], e4m3x2_to_f16x2_scaled<kSel02>(R2) & vm01,
-                                    e4m3x2_to_f16x2_scaled<kSel13>(R2) & vm01, e4m3x2_to_f16x2_scaled<kSel02>(R3) & vm23,
-                                    e4m3x2_to_f16x2_scaled<kSel13>(R3) & vm23, pb0, pb1);
+                            // byte pairs (0, 2) and (1, 3) of each word, gathered by one permute
+                            const uint32_t T0 = prmt(R0, 0x3120u), T1 = prmt(R1, 0x3120u);
+                            const uint32_t T2 = prmt(R2, 0x3120u), T3 = prmt(R3, 0x3120u);
+                            mma_f16(oo[2 * j2], e4m3x2_to_f16x2(T0) & vm01, e4m3x2_to_f16x2(T0 >> 16) & vm01,
+                                    e4m3x2_to_f16x2(T1) & vm23, e4m3x2_to_f16x2(T1 >> 16) & vm23, pb0, pb1);
+                            mma_f16(oo[2 * j2 + 1], e4m3x2_to_f16x2(T2) & vm01, e4m3x2_to_f16x2(T2 >> 16) & vm01,
+                                    e4m3x2_to_f16x2(T3) & vm23, e4m3x2_to_f16x2(T3 >> 16) & vm23, pb0, pb1);
                         }
                     } else {
 #pragma unroll

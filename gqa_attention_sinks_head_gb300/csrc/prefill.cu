@@ -110,15 +110,6 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t x)
     return pack_f16(__uint_as_float(x << 16), __uint_as_float(x & 0xffff0000u));
 }
 
-// Two E4M3 codes (low byte first) -> their values as f16x2 (exact: every
-// E4M3 value, subnormals included, is an f16 normal).
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes)
-{
-    uint32_t d;
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"(static_cast<unsigned short>(two_codes)));
-    return d;
-}
-
 // One key tile of E4M3 codes (64 rows of 64 bytes as TMA wrote them with the
 // 64-byte swizzle: 16-byte chunk c of row r at chunk c ^ ((r >> 1) & 3)) ->
 // f16 values in the 128-byte-swizzled layout of a 16-bit tile (chunk c of row

@@ -32,7 +32,7 @@ struct DecodeParams {
     int32_t partial;           // 1: write sink-free partial states; 0: final output
     int32_t dim_token, dim_head, dim_page;  // tensor-map dimension (1..3) of each coordinate
     float score_scale;         // multiplies q.k to give base-2 logits
-    float out_scale;           // multiplies the normalised value sum (FP8: v_scale * 2^8)
+    float out_scale;           // multiplies the normalised value sum (FP8: v_scale)
 };
 
 struct MergeParams {

@@ -213,23 +213,15 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t sel)
     return d;
 }
 
-// Two E4M3 codes -> f16x2 holding code_value * 2^-8, exactly (subnormal codes
-// become f16 subnormals).  The selector picks the two bytes of `w` (low result
-// half first) and replicates each byte's sign bit into the byte above it; a
-// 7-bit left shift then places sign, exponent and mantissa in f16 position:
-// the 4 exponent bits land in the low bits of the f16 exponent, which rebiases
-// 7 -> 15 (a factor 2^-8), and the mask drops the bits that leaked from the
-// neighbouring byte.  Codes 0x7F/0xFF (NaN in E4M3) come out as +-480 * 2^-8.
-template <uint32_t SEL>
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2_scaled(uint32_t w)
+// Two E4M3 codes (the low 16 bits of w, lowest byte first) -> their values as
+// f16x2, exactly: every E4M3 value, subnormals included, is an f16 normal.
+// Codes 0x7F / 0xFF (NaN in E4M3) give f16 NaN.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t w)
 {
-    return (prmt(w, SEL) << 7) & 0xBF80BF80u;
+    uint32_t d;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"(static_cast<unsigned short>(w)));
+    return d;
 }
-// selectors: byte pair (0,1), (2,3), (0,2), (1,3)
-constexpr uint32_t kSel01 = 0x9180u;
-constexpr uint32_t kSel23 = 0xB3A2u;
-constexpr uint32_t kSel02 = 0xA280u;
-constexpr uint32_t kSel13 = 0xB391u;
 
 }  // namespace sa
 
