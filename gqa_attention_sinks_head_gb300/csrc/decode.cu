@@ -36,10 +36,11 @@
 // Multi-token decode (q_len 2..8 new tokens per sequence, as a speculative or
 // multi-token-prediction verifier sends them; "GPT-OSS on day 0", the engine's
 // speculative and MTP decoders): token k of sequence b sits at position
-// L_b - q_len + k.  Each consumer warp owns one token (q_len <= 4; the warps
-// that share a token take turns over the tiles of a stage) or two (q_len 5..8,
-// TPW = 2; every warp then reads all four tiles of a stage), so the block still
-// reads each K/V byte of the kv head once for all tokens and heads.
+// L_b - q_len + k.  Each consumer warp owns one token (q_len <= 4) or two
+// (TPW = 2, q_len 5..8: two softmax chains interleaved on the same K/V
+// fragments); the warps that own the same tokens take turns over the tiles of
+// a stage.  The block still reads each K/V byte of the kv head once for all
+// tokens and heads.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -138,13 +139,16 @@ __global__ void __launch_bounds__(kThreads, TPW == 1 ? 4 : 3) decode_kernel(cons
     }
     __syncthreads();
 
-    // Token slots of this consumer warp.  TPW 1: token warp % qlen, shared by
-    // `rep` warps that take the stage's tiles j with j % rep == warp / qlen.
-    // TPW 2: tokens warp and warp + 4, every tile of the stage.
-    const int tok0_w = TPW == 1 ? (qlen > 0 ? warp % qlen : 0) : warp;
-    const int rep = TPW == 1 ? (kConsumerWarps - 1 - tok0_w) / max(qlen, 1) + 1 : 1;
-    const int rep_idx = TPW == 1 ? warp / max(qlen, 1) : 0;
-    const int ntok = TPW == 1 ? 1 : (warp + 4 < qlen ? 2 : 1);
+    // Token slots of this consumer warp.  The qlen tokens form G = ceil(qlen /
+    // TPW) groups, group g holding tokens g, g + G, ..; warp w takes group
+    // w % G, and the `rep` warps that share a group take the stage's tiles j
+    // with j % rep == w / G.  Two tokens per warp (TPW 2) interleave two
+    // independent softmax chains on the same K/V fragments.
+    const int ngroups = max((qlen + TPW - 1) / TPW, 1);
+    const int tok0_w = warp % ngroups;
+    const int rep = (kConsumerWarps - 1 - tok0_w) / ngroups + 1;
+    const int rep_idx = warp / ngroups;
+    const int ntok = (TPW == 2 && tok0_w + ngroups < qlen) ? 2 : 1;
 
     // consumer state (per token slot), kept past the role split for the block-level merge
     float m[TPW][2], l[TPW][2], o[TPW][4][4];
@@ -214,7 +218,7 @@ __global__ void __launch_bounds__(kThreads, TPW == 1 ? 4 : 3) decode_kernel(cons
         int tf[TPW], te[TPW];
 #pragma unroll
         for (int tt = 0; tt < TPW; ++tt) {
-            const int tok = tok0_w + 4 * tt;
+            const int tok = tok0_w + ngroups * tt;
             const int hi_k = L - qlen + tok + 1;  // one past the token's own position
             const int lo_k = p.window > 0 ? max(0, hi_k - p.window) : 0;
             tf[tt] = max(t_first, lo_k);
@@ -439,10 +443,10 @@ __global__ void __launch_bounds__(kThreads, TPW == 1 ? 4 : 3) decode_kernel(cons
         const int n = threadIdx.x >> 4;
         const int d0 = (threadIdx.x & 15) * 4;
         for (int k = 0; k < qlen && n < p.group; ++k) {
-            // slots holding token k: TPW 1: warps w with w % qlen == k; TPW 2: (k % 4, k / 4)
-            const int w0 = TPW == 1 ? k : k % 4;
-            const int wstep = TPW == 1 ? qlen : kConsumerWarps;
-            const int tt = TPW == 1 ? 0 : k / 4;
+            // slots holding token k: slot k / G of the warps w with w % G == k % G
+            const int w0 = k % ngroups;
+            const int wstep = ngroups;
+            const int tt = k / ngroups;
             float M = -INFINITY;
             for (int w = w0; w < kConsumerWarps; w += wstep)
                 M = fmaxf(M, sm.red_m[w][tt][n]);
@@ -539,7 +543,10 @@ cudaError_t decode_occupancy(bool fp8, int *blocks_per_sm)
 cudaError_t launch_decode(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p, bool fp8,
                           cudaStream_t stream)
 {
-    if (p.q_len > 4)  // two tokens per consumer warp
+    // two tokens per consumer warp past four tokens (measured: for q_len 2..4
+    // the fourth block per SM that one token per warp allows is worth more than
+    // the second chain)
+    if (p.q_len > 4)
         return fp8 ? launch_of<true, 2 * kDefaultStages, 2>(tk, tv, p, stream)
                    : launch_of<false, kDefaultStages, 2>(tk, tv, p, stream);
     return fp8 ? launch_of<true, 2 * kDefaultStages, 1>(tk, tv, p, stream)
