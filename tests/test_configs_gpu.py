@@ -85,3 +85,36 @@ def test_config7_chunked_paged_prefill_fp8(sa, oracle):
                                     g.choice(8192, 48, replace=False)])).astype(np.int32)
     ref_o, ref_l = oracle_prefill(oracle, case, sel)
     check_close(out[sel], lse[sel], ref_o, ref_l, "config 7")
+
+
+@pytest.mark.parametrize("window", [0, 128])
+def test_long_context_128k(sa, oracle, window):
+    """The model's 128k context: one decode query and a 64-query chunk at the
+    end of a 131072-key paged cache (P=16, 8192 pages per sequence), every
+    output compared.  Exercises large page tables, many split chunks and
+    positions past 2^16."""
+    from sa_testlib import oracle_prefill, prefill_gpu
+    L = 131072
+    case = W.make_decode_case([L, 5000], page_size=16, paged=True, window=window, seed=130, device="cuda")
+    assert sa.sa_decode_num_splits(2, 8, L, window) >= (1 if window else 16)
+    out, lse = decode_gpu(sa, case)
+    assert sa.sa_device_status() == 0
+    _sampled(oracle, case, out, lse, [0, 1], "decode 128k w=%d" % window)
+    pcase = W.make_prefill_case([64], [L], paged=True, page_size=16, layout="HND", window=window, seed=131)
+    pout, plse = prefill_gpu(sa, pcase.to("cuda"))
+    assert sa.sa_device_status() == 0
+    sel = np.array([0, 1, 31, 62, 63], dtype=np.int32)
+    ref_o, ref_l = oracle_prefill(oracle, pcase, sel)
+    check_close(pout[sel], plse[sel], ref_o, ref_l, "prefill chunk at 128k w=%d" % window)
+
+
+def test_large_batch_of_short_sequences(sa, oracle):
+    """5000 sequences of 0..40 keys (empty ones included), paged: a grid
+    z-extent in the thousands and many empty slots; every output compared."""
+    g = np.random.default_rng(132)
+    lens = g.integers(0, 41, 5000).tolist()
+    case = W.make_decode_case(lens, page_size=16, paged=True, poison_pages=7, seed=132)
+    out, lse = decode_gpu(sa, case.to("cuda"))
+    assert sa.sa_device_status() == 0
+    ref_o, ref_l = oracle_decode(oracle, case)
+    check_close(out, lse, ref_o, ref_l, "B=5000 short")
