@@ -45,6 +45,7 @@
 #include <cuda_fp16.h>
 
 #include <cstdlib>
+#include <type_traits>
 
 #include "sa_internal.h"
 #include "sa_ptx.cuh"
@@ -376,28 +377,39 @@ __global__ void __launch_bounds__(kThreads, TPW == 1 ? 4 : 3) decode_kernel(cons
                     }
 
                     // ---- O^T += V^T . P^T ---------------------------------------
-                    if constexpr (FP8) {
+                    // Value rows outside the tile's visible range are zeroed (vm01,
+                    // vm23) on edge tiles only; interior tiles skip the masks.
+                    auto pv = [&](auto masked) {
+                        constexpr bool kMasked = decltype(masked)::value;
+                        auto mk = [&](uint32_t x, uint32_t vm) { return kMasked ? (x & vm) : x; };
+                        if constexpr (FP8) {
 #pragma unroll
-                        for (int j2 = 0; j2 < 2; ++j2) {
-                            uint32_t R0, R1, R2, R3;
-                            ldsm_x4_t(vt + swz<true>((mi & 1) * 8 + lr, 2 * j2 + (mi >> 1)), R0, R1, R2, R3);
-                            // rows of m-tile 2*j2 (+1): row r <-> dim 16ch + 2r, row r+8 <-> 16ch + 2r + 1
-                            // byte pairs (0, 2) and (1, 3) of each word, gathered by one permute
-                            const uint32_t T0 = prmt(R0, 0x3120u), T1 = prmt(R1, 0x3120u);
-                            const uint32_t T2 = prmt(R2, 0x3120u), T3 = prmt(R3, 0x3120u);
-                            mma_f16(oo[2 * j2], e4m3x2_to_f16x2(T0) & vm01, e4m3x2_to_f16x2(T0 >> 16) & vm01,
-                                    e4m3x2_to_f16x2(T1) & vm23, e4m3x2_to_f16x2(T1 >> 16) & vm23, pb0, pb1);
-                            mma_f16(oo[2 * j2 + 1], e4m3x2_to_f16x2(T2) & vm01, e4m3x2_to_f16x2(T2 >> 16) & vm01,
-                                    e4m3x2_to_f16x2(T3) & vm23, e4m3x2_to_f16x2(T3 >> 16) & vm23, pb0, pb1);
-                        }
-                    } else {
+                            for (int j2 = 0; j2 < 2; ++j2) {
+                                uint32_t R0, R1, R2, R3;
+                                ldsm_x4_t(vt + swz<true>((mi & 1) * 8 + lr, 2 * j2 + (mi >> 1)), R0, R1, R2, R3);
+                                // rows of m-tile 2*j2 (+1): row r <-> dim 16ch + 2r, row r+8 <-> 16ch + 2r + 1;
+                                // byte pairs (0, 2) and (1, 3) of each word, gathered by one permute
+                                const uint32_t T0 = prmt(R0, 0x3120u), T1 = prmt(R1, 0x3120u);
+                                const uint32_t T2 = prmt(R2, 0x3120u), T3 = prmt(R3, 0x3120u);
+                                mma_f16(oo[2 * j2], mk(e4m3x2_to_f16x2(T0), vm01), mk(e4m3x2_to_f16x2(T0 >> 16), vm01),
+                                        mk(e4m3x2_to_f16x2(T1), vm23), mk(e4m3x2_to_f16x2(T1 >> 16), vm23), pb0, pb1);
+                                mma_f16(oo[2 * j2 + 1], mk(e4m3x2_to_f16x2(T2), vm01),
+                                        mk(e4m3x2_to_f16x2(T2 >> 16), vm01), mk(e4m3x2_to_f16x2(T3), vm23),
+                                        mk(e4m3x2_to_f16x2(T3 >> 16), vm23), pb0, pb1);
+                            }
+                        } else {
 #pragma unroll
-                        for (int mt = 0; mt < 4; ++mt) {
-                            uint32_t a0, a1, a2, a3;
-                            ldsm_x4_t(vt + swz<false>((mi >> 1) * 8 + lr, 2 * mt + (mi & 1)), a0, a1, a2, a3);
-                            mma_bf16(oo[mt], a0 & vm01, a1 & vm01, a2 & vm23, a3 & vm23, pb0, pb1);
+                            for (int mt = 0; mt < 4; ++mt) {
+                                uint32_t a0, a1, a2, a3;
+                                ldsm_x4_t(vt + swz<false>((mi >> 1) * 8 + lr, 2 * mt + (mi & 1)), a0, a1, a2, a3);
+                                mma_bf16(oo[mt], mk(a0, vm01), mk(a1, vm01), mk(a2, vm23), mk(a3, vm23), pb0, pb1);
+                            }
                         }
-                    }
+                    };
+                    if (edge)
+                        pv(std::true_type{});
+                    else
+                        pv(std::false_type{});
                 }
             }
             __syncwarp();
