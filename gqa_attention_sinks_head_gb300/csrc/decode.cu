@@ -289,11 +289,14 @@ __global__ void __launch_bounds__(kThreads, TPW == 1 ? 4 : 3) decode_kernel(cons
                         for (int j2 = 0; j2 < 2; ++j2) {
                             uint32_t R0, R1, R2, R3;
                             ldsm_x4(kt + swz<true>((mi & 1) * 8 + lr, 2 * j2 + (mi >> 1)), R0, R1, R2, R3);
-                            mma_f16(s, e4m3x2_to_f16x2(R0), e4m3x2_to_f16x2(R1), e4m3x2_to_f16x2(R0 >> 16),
-                                    e4m3x2_to_f16x2(R1 >> 16),
+                            uint32_t k0l, k0h, k1l, k1h;
+                            e4m3x4_to_f16x2x2(R0, k0l, k0h);
+                            e4m3x4_to_f16x2x2(R1, k1l, k1h);
+                            mma_f16(s, k0l, k1l, k0h, k1h,
                                     qf[tt][2 * j2][0], qf[tt][2 * j2][1]);
-                            mma_f16(s, e4m3x2_to_f16x2(R2), e4m3x2_to_f16x2(R3), e4m3x2_to_f16x2(R2 >> 16),
-                                    e4m3x2_to_f16x2(R3 >> 16),
+                            e4m3x4_to_f16x2x2(R2, k0l, k0h);
+                            e4m3x4_to_f16x2x2(R3, k1l, k1h);
+                            mma_f16(s, k0l, k1l, k0h, k1h,
                                     qf[tt][2 * j2 + 1][0], qf[tt][2 * j2 + 1][1]);
                         }
                     } else {
@@ -389,13 +392,15 @@ __global__ void __launch_bounds__(kThreads, TPW == 1 ? 4 : 3) decode_kernel(cons
                                 ldsm_x4_t(vt + swz<true>((mi & 1) * 8 + lr, 2 * j2 + (mi >> 1)), R0, R1, R2, R3);
                                 // rows of m-tile 2*j2 (+1): row r <-> dim 16ch + 2r, row r+8 <-> 16ch + 2r + 1;
                                 // byte pairs (0, 2) and (1, 3) of each word, gathered by one permute
-                                const uint32_t T0 = prmt(R0, 0x3120u), T1 = prmt(R1, 0x3120u);
-                                const uint32_t T2 = prmt(R2, 0x3120u), T3 = prmt(R3, 0x3120u);
-                                mma_f16(oo[2 * j2], mk(e4m3x2_to_f16x2(T0), vm01), mk(e4m3x2_to_f16x2(T0 >> 16), vm01),
-                                        mk(e4m3x2_to_f16x2(T1), vm23), mk(e4m3x2_to_f16x2(T1 >> 16), vm23), pb0, pb1);
-                                mma_f16(oo[2 * j2 + 1], mk(e4m3x2_to_f16x2(T2), vm01),
-                                        mk(e4m3x2_to_f16x2(T2 >> 16), vm01), mk(e4m3x2_to_f16x2(T3), vm23),
-                                        mk(e4m3x2_to_f16x2(T3 >> 16), vm23), pb0, pb1);
+                                uint32_t v0l, v0h, v1l, v1h, v2l, v2h, v3l, v3h;
+                                e4m3x4_to_f16x2x2(prmt(R0, 0x3120u), v0l, v0h);
+                                e4m3x4_to_f16x2x2(prmt(R1, 0x3120u), v1l, v1h);
+                                e4m3x4_to_f16x2x2(prmt(R2, 0x3120u), v2l, v2h);
+                                e4m3x4_to_f16x2x2(prmt(R3, 0x3120u), v3l, v3h);
+                                mma_f16(oo[2 * j2], mk(v0l, vm01), mk(v0h, vm01), mk(v1l, vm23), mk(v1h, vm23), pb0,
+                                        pb1);
+                                mma_f16(oo[2 * j2 + 1], mk(v2l, vm01), mk(v2h, vm01), mk(v3l, vm23), mk(v3h, vm23),
+                                        pb0, pb1);
                             }
                         } else {
 #pragma unroll

@@ -123,14 +123,10 @@ __device__ __forceinline__ void widen_tile(const uint8_t *src, uint8_t *dst, int
         if (r < valid)
             w = *reinterpret_cast<const uint4 *>(src + r * 64 + ((c ^ ((r >> 1) & 3)) << 4));
         uint4 lo, hi;
-        lo.x = e4m3x2_to_f16x2(w.x);
-        lo.y = e4m3x2_to_f16x2(w.x >> 16);
-        lo.z = e4m3x2_to_f16x2(w.y);
-        lo.w = e4m3x2_to_f16x2(w.y >> 16);
-        hi.x = e4m3x2_to_f16x2(w.z);
-        hi.y = e4m3x2_to_f16x2(w.z >> 16);
-        hi.z = e4m3x2_to_f16x2(w.w);
-        hi.w = e4m3x2_to_f16x2(w.w >> 16);
+        e4m3x4_to_f16x2x2(w.x, lo.x, lo.y);
+        e4m3x4_to_f16x2x2(w.y, lo.z, lo.w);
+        e4m3x4_to_f16x2x2(w.z, hi.x, hi.y);
+        e4m3x4_to_f16x2x2(w.w, hi.z, hi.w);
         *reinterpret_cast<uint4 *>(dst + r * 128 + (((2 * c) ^ (r & 7)) << 4)) = lo;
         *reinterpret_cast<uint4 *>(dst + r * 128 + (((2 * c + 1) ^ (r & 7)) << 4)) = hi;
     }

@@ -223,6 +223,17 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t w)
     return d;
 }
 
+// Four E4M3 codes (bytes 0..3 of w) -> two f16x2: bytes (0, 1) in lo, (2, 3) in hi.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t &lo, uint32_t &hi)
+{
+    asm("{\n\t.reg .b16 a, b;\n\t"
+        "mov.b32 {a, b}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, a;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
+}
+
 }  // namespace sa
 
 // ====================================================================
