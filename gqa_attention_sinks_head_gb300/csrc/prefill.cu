@@ -37,7 +37,7 @@
 // are applied only on tiles that straddle a boundary.
 //
 // FP8-E4M3 caches (vLLM "GPT-OSS optimisations on NVIDIA Blackwell", FP8 KV
-// cache): TMA brings each key tile's E4M3 codes into a 2-slot staging area,
+// cache): TMA brings each key tile's E4M3 codes into a 4-slot staging area,
 // and the producer warp widens them (cvt e4m3x2 -> f16x2, exact for every
 // code) into the same f16 tiles (128-byte swizzle) the MMAs read, zeroing
 // rows past the sequence end.  The softmax warps convert their Q tile from
