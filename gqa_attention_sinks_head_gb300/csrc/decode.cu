@@ -71,6 +71,10 @@ struct DecodeCfg {
 };
 
 constexpr int kMaxTPW = 2;  // query tokens per consumer warp (q_len <= 8)
+// Row stride (floats) of the block-merge scratch [slot][head][dim]: 4 floats of
+// padding put the 8 heads of a warp's float4 reads and of the fragment writes
+// in different banks.
+constexpr int kRedStride = kHeadDim + 4;
 
 template <bool FP8, int kStages>
 struct DecodeSmem {
@@ -93,15 +97,18 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk)
         return row * 128 + ((chunk ^ (row & 7)) << 4);
 }
 
-template <bool FP8, int kStages, int TPW>
+// kJoint: a warp that owns several tiles of a stage (2..4 query tokens) runs
+// them as one block; the one-token kernel is built without that path.
+template <bool FP8, int kStages, int TPW, bool kJoint>
 __global__ void __launch_bounds__(kThreads, TPW == 1 ? 4 : 3) decode_kernel(const __grid_constant__ CUtensorMap tmk,
                                                                           const __grid_constant__ CUtensorMap tmv,
                                                                           const DecodeParams p)
 {
     using Cfg = DecodeCfg<FP8>;
+    static_assert(!kJoint || TPW == 1, "joint tiles are built for one token per warp");
     extern __shared__ uint8_t smem_raw[];
     // the per-warp O^T partials of the final merge reuse the K tiles
-    static_assert(sizeof(float) * kConsumerWarps * TPW * kHeadDim * kMaxGroup <=
+    static_assert(sizeof(float) * kConsumerWarps * TPW * kMaxGroup * kRedStride <=
                       sizeof(uint8_t) * kStages * kConsumerWarps * Cfg::kTileBytes,
                   "merge scratch must fit in the K tiles");
     DecodeSmem<FP8, kStages> &sm =
@@ -262,134 +269,181 @@ __global__ void __launch_bounds__(kThreads, TPW == 1 ? 4 : 3) decode_kernel(cons
         }
         const int lr = lane & 7;
         const int mi = lane >> 3;
-        for (int st = 0; st < nstages; ++st) {
-            const int buf = st % kStages;
-            if (!mbar_wait(&sm.full[buf], (st / kStages) & 1, p.status))
-                break;
-            for (int j = rep_idx; j < kConsumerWarps; j += rep) {
-                const int tile = st * kConsumerWarps + j;
-                if (tile >= ntiles)
-                    break;
-                const int tok0 = t_begin + tile * kTile;
-                const uint32_t kt = smem_u32(sm.k[buf][j]);
-                const uint32_t vt = smem_u32(sm.v[buf][j]);
+        // Tiles j0, j0 + jstep, .. (NT of them) of stage buffer buf, taken as one
+        // block of NT x 16 keys: NT independent score products, one max / rescale
+        // decision and one softmax pass, then NT value products.  NT > 1 gives a
+        // warp that owns several tiles of a stage (multi-token decode) NT
+        // independent dependency chains instead of NT chains in a row.
+        auto run_tiles = [&](auto ntc, int buf, int st, int j0, int jstep) {
+            constexpr int NT = decltype(ntc)::value;
+            int tok0[NT];
+            uint32_t kt[NT], vt[NT];
 #pragma unroll
-                for (int tt = 0; tt < TPW; ++tt) {
-                    if (tt >= ntok || tok0 + kTile <= tf[tt] || tok0 >= te[tt])
-                        continue;  // no key of this tile is visible to the token
-                    const int t_first = tf[tt], t_end = te[tt];
-                    float (&mm)[2] = m[tt];
-                    float (&ll)[2] = l[tt];
-                    float (&oo)[4][4] = o[tt];
+            for (int i = 0; i < NT; ++i) {
+                const int j = j0 + i * jstep;
+                tok0[i] = t_begin + (st * kConsumerWarps + j) * kTile;
+                kt[i] = smem_u32(sm.k[buf][j]);
+                vt[i] = smem_u32(sm.v[buf][j]);
+            }
+#pragma unroll
+            for (int tt = 0; tt < TPW; ++tt) {
+                const int t_first = tf[tt], t_end = te[tt];
+                bool vis = false, edge = false;
+#pragma unroll
+                for (int i = 0; i < NT; ++i) {
+                    vis |= tok0[i] + kTile > t_first && tok0[i] < t_end;
+                    edge |= tok0[i] < t_first || tok0[i] + kTile > t_end;
+                }
+                if (tt >= ntok || !vis)
+                    continue;  // no key of these tiles is visible to the token
+                float (&mm)[2] = m[tt];
+                float (&ll)[2] = l[tt];
+                float (&oo)[4][4] = o[tt];
 
-                    // ---- S^T = K . Q^T  (16 keys x 8 heads, fp32) --------------
-                    float s[4] = {0.f, 0.f, 0.f, 0.f};
+                // ---- S^T = K . Q^T  (16 keys x 8 heads per tile, fp32) ----------
+                float s[NT][4];
+#pragma unroll
+                for (int i = 0; i < NT; ++i) {
+                    s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
                     if constexpr (FP8) {
 #pragma unroll
                         for (int j2 = 0; j2 < 2; ++j2) {
                             uint32_t R0, R1, R2, R3;
-                            ldsm_x4(kt + swz<true>((mi & 1) * 8 + lr, 2 * j2 + (mi >> 1)), R0, R1, R2, R3);
+                            ldsm_x4(kt[i] + swz<true>((mi & 1) * 8 + lr, 2 * j2 + (mi >> 1)), R0, R1, R2, R3);
                             uint32_t k0l, k0h, k1l, k1h;
                             e4m3x4_to_f16x2x2(R0, k0l, k0h);
                             e4m3x4_to_f16x2x2(R1, k1l, k1h);
-                            mma_f16(s, k0l, k1l, k0h, k1h,
-                                    qf[tt][2 * j2][0], qf[tt][2 * j2][1]);
+                            mma_f16(s[i], k0l, k1l, k0h, k1h, qf[tt][2 * j2][0], qf[tt][2 * j2][1]);
                             e4m3x4_to_f16x2x2(R2, k0l, k0h);
                             e4m3x4_to_f16x2x2(R3, k1l, k1h);
-                            mma_f16(s, k0l, k1l, k0h, k1h,
-                                    qf[tt][2 * j2 + 1][0], qf[tt][2 * j2 + 1][1]);
+                            mma_f16(s[i], k0l, k1l, k0h, k1h, qf[tt][2 * j2 + 1][0], qf[tt][2 * j2 + 1][1]);
                         }
                     } else {
 #pragma unroll
                         for (int ks = 0; ks < 4; ++ks) {
                             uint32_t a0, a1, a2, a3;
-                            ldsm_x4(kt + swz<false>((mi & 1) * 8 + lr, 2 * ks + (mi >> 1)), a0, a1, a2, a3);
-                            mma_bf16(s, a0, a1, a2, a3, qf[tt][ks][0], qf[tt][ks][1]);
+                            ldsm_x4(kt[i] + swz<false>((mi & 1) * 8 + lr, 2 * ks + (mi >> 1)), a0, a1, a2, a3);
+                            mma_bf16(s[i], a0, a1, a2, a3, qf[tt][ks][0], qf[tt][ks][1]);
                         }
                     }
+                }
 
-                    // ---- online softmax (base 2) -------------------------------
-                    // s[0]: key r, head 2c   s[1]: key r, head 2c+1
-                    // s[2]: key r+8, head 2c s[3]: key r+8, head 2c+1
+                // ---- online softmax (base 2) -----------------------------------
+                // s[i][0]: key r, head 2c   s[i][1]: key r, head 2c+1
+                // s[i][2]: key r+8, head 2c s[i][3]: key r+8, head 2c+1
 #pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        s[i] *= p.score_scale;
-                    const bool edge = tok0 < t_first || tok0 + kTile > t_end;
-                    uint32_t vm01 = 0xffffffffu, vm23 = 0xffffffffu;
-                    if (edge) {
-                        const bool v0 = tok0 + r >= t_first && tok0 + r < t_end;
-                        const bool v8 = tok0 + r + 8 >= t_first && tok0 + r + 8 < t_end;
-                        s[0] = v0 ? s[0] : -INFINITY;
-                        s[1] = v0 ? s[1] : -INFINITY;
-                        s[2] = v8 ? s[2] : -INFINITY;
-                        s[3] = v8 ? s[3] : -INFINITY;
+                for (int i = 0; i < NT; ++i)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        s[i][e] *= p.score_scale;
+                uint32_t vm01[NT], vm23[NT];
+#pragma unroll
+                for (int i = 0; i < NT; ++i)
+                    vm01[i] = vm23[i] = 0xffffffffu;
+                if (edge) {
+#pragma unroll
+                    for (int i = 0; i < NT; ++i) {
+                        const bool v0 = tok0[i] + r >= t_first && tok0[i] + r < t_end;
+                        const bool v8 = tok0[i] + r + 8 >= t_first && tok0[i] + r + 8 < t_end;
+                        s[i][0] = v0 ? s[i][0] : -INFINITY;
+                        s[i][1] = v0 ? s[i][1] : -INFINITY;
+                        s[i][2] = v8 ? s[i][2] : -INFINITY;
+                        s[i][3] = v8 ? s[i][3] : -INFINITY;
                         // value rows outside the range are zeroed (a NaN there must not leak via 0 * NaN)
-                        const int k0 = tok0 + 2 * c, k8 = tok0 + 2 * c + 8;
-                        vm01 = ((k0 >= t_first && k0 < t_end) ? 0x0000ffffu : 0u) |
-                               ((k0 + 1 >= t_first && k0 + 1 < t_end) ? 0xffff0000u : 0u);
-                        vm23 = ((k8 >= t_first && k8 < t_end) ? 0x0000ffffu : 0u) |
-                               ((k8 + 1 >= t_first && k8 + 1 < t_end) ? 0xffff0000u : 0u);
+                        const int k0 = tok0[i] + 2 * c, k8 = tok0[i] + 2 * c + 8;
+                        vm01[i] = ((k0 >= t_first && k0 < t_end) ? 0x0000ffffu : 0u) |
+                                  ((k0 + 1 >= t_first && k0 + 1 < t_end) ? 0xffff0000u : 0u);
+                        vm23[i] = ((k8 >= t_first && k8 < t_end) ? 0x0000ffffu : 0u) |
+                                  ((k8 + 1 >= t_first && k8 + 1 < t_end) ? 0xffff0000u : 0u);
                     }
-                    // The running max moves only when some score of the tile exceeds it
-                    // by more than kRescaleThreshold (log2 units): p stays below 2^8,
-                    // the result is unchanged (numerator and denominator share m), and
-                    // most tiles skip the cross-lane max and the O rescale.
-                    float mx0 = fmaxf(s[0], s[2]);
-                    float mx1 = fmaxf(s[1], s[3]);
-                    // (-inf - -inf is NaN: a lane with nothing visible never asks)
-                    const bool grow = mx0 - mm[0] > kRescaleThreshold || mx1 - mm[1] > kRescaleThreshold;
-                    if (__any_sync(0xffffffffu, grow)) {
+                }
+                // The running max moves only when some score of the block exceeds it
+                // by more than kRescaleThreshold (log2 units): p stays below 2^8,
+                // the result is unchanged (numerator and denominator share m), and
+                // most blocks skip the cross-lane max and the O rescale.
+                float tm0[NT], tm1[NT];  // per-tile maxima, reduced as a tree
 #pragma unroll
-                        for (int off = 4; off < 32; off <<= 1) {
-                            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-                            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-                        }
-                        const float mn0 = fmaxf(mm[0], mx0);
-                        const float mn1 = fmaxf(mm[1], mx1);
-                        // alpha = 0 from m = -inf (l and O are still 0); 1 while nothing is visible
-                        const float al0 = mn0 == -INFINITY ? 1.f : ex2(mm[0] - mn0);
-                        const float al1 = mn1 == -INFINITY ? 1.f : ex2(mm[1] - mn1);
-                        ll[0] *= al0;
-                        ll[1] *= al1;
-                        mm[0] = mn0;
-                        mm[1] = mn1;
+                for (int i = 0; i < NT; ++i) {
+                    tm0[i] = fmaxf(s[i][0], s[i][2]);
+                    tm1[i] = fmaxf(s[i][1], s[i][3]);
+                }
 #pragma unroll
-                        for (int mt = 0; mt < 4; ++mt) {
-                            oo[mt][0] *= al0;
-                            oo[mt][1] *= al1;
-                            oo[mt][2] *= al0;
-                            oo[mt][3] *= al1;
-                        }
+                for (int w = 1; w < NT; w *= 2)
+#pragma unroll
+                    for (int i = 0; i + w < NT; i += 2 * w) {
+                        tm0[i] = fmaxf(tm0[i], tm0[i + w]);
+                        tm1[i] = fmaxf(tm1[i], tm1[i + w]);
                     }
-                    const float mu0 = mm[0] == -INFINITY ? 0.f : mm[0];  // keep exp2 finite
-                    const float mu1 = mm[1] == -INFINITY ? 0.f : mm[1];
-                    const float p0 = ex2(s[0] - mu0);
-                    const float p1 = ex2(s[1] - mu1);
-                    const float p2 = ex2(s[2] - mu0);
-                    const float p3 = ex2(s[3] - mu1);
-                    ll[0] += p0 + p2;
-                    ll[1] += p1 + p3;
-                    // P (key-major C layout) -> P^T as the B operand (K = keys, N = heads)
-                    uint32_t pb0, pb1;
+                float mx0 = tm0[0], mx1 = tm1[0];
+                // (-inf - -inf is NaN: a lane with nothing visible never asks)
+                const bool grow = mx0 - mm[0] > kRescaleThreshold || mx1 - mm[1] > kRescaleThreshold;
+                if (__any_sync(0xffffffffu, grow)) {
+#pragma unroll
+                    for (int off = 4; off < 32; off <<= 1) {
+                        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+                    }
+                    const float mn0 = fmaxf(mm[0], mx0);
+                    const float mn1 = fmaxf(mm[1], mx1);
+                    // alpha = 0 from m = -inf (l and O are still 0); 1 while nothing is visible
+                    const float al0 = mn0 == -INFINITY ? 1.f : ex2(mm[0] - mn0);
+                    const float al1 = mn1 == -INFINITY ? 1.f : ex2(mm[1] - mn1);
+                    ll[0] *= al0;
+                    ll[1] *= al1;
+                    mm[0] = mn0;
+                    mm[1] = mn1;
+#pragma unroll
+                    for (int mt = 0; mt < 4; ++mt) {
+                        oo[mt][0] *= al0;
+                        oo[mt][1] *= al1;
+                        oo[mt][2] *= al0;
+                        oo[mt][3] *= al1;
+                    }
+                }
+                const float mu0 = mm[0] == -INFINITY ? 0.f : mm[0];  // keep exp2 finite
+                const float mu1 = mm[1] == -INFINITY ? 0.f : mm[1];
+                // P (key-major C layout) -> P^T as the B operand (K = keys, N = heads)
+                uint32_t pb[NT][2];
+                float ps0[NT], ps1[NT];  // per-tile sums of p, reduced as a tree
+#pragma unroll
+                for (int i = 0; i < NT; ++i) {
+                    const float p0 = ex2(s[i][0] - mu0);
+                    const float p1 = ex2(s[i][1] - mu1);
+                    const float p2 = ex2(s[i][2] - mu0);
+                    const float p3 = ex2(s[i][3] - mu1);
+                    ps0[i] = p0 + p2;
+                    ps1[i] = p1 + p3;
                     if constexpr (FP8) {
-                        pb0 = movmatrix_t(pack_f16(p0, p1));
-                        pb1 = movmatrix_t(pack_f16(p2, p3));
+                        pb[i][0] = movmatrix_t(pack_f16(p0, p1));
+                        pb[i][1] = movmatrix_t(pack_f16(p2, p3));
                     } else {
-                        pb0 = movmatrix_t(pack_bf16(p0, p1));
-                        pb1 = movmatrix_t(pack_bf16(p2, p3));
+                        pb[i][0] = movmatrix_t(pack_bf16(p0, p1));
+                        pb[i][1] = movmatrix_t(pack_bf16(p2, p3));
                     }
+                }
+#pragma unroll
+                for (int w = 1; w < NT; w *= 2)
+#pragma unroll
+                    for (int i = 0; i + w < NT; i += 2 * w) {
+                        ps0[i] += ps0[i + w];
+                        ps1[i] += ps1[i + w];
+                    }
+                ll[0] += ps0[0];
+                ll[1] += ps1[0];
 
-                    // ---- O^T += V^T . P^T ---------------------------------------
-                    // Value rows outside the tile's visible range are zeroed (vm01,
-                    // vm23) on edge tiles only; interior tiles skip the masks.
-                    auto pv = [&](auto masked) {
-                        constexpr bool kMasked = decltype(masked)::value;
+                // ---- O^T += V^T . P^T -------------------------------------------
+                // Value rows outside a tile's visible range are zeroed (vm01, vm23)
+                // on edge blocks only; interior blocks skip the masks.
+                auto pv = [&](auto masked) {
+                    constexpr bool kMasked = decltype(masked)::value;
+#pragma unroll
+                    for (int i = 0; i < NT; ++i) {
                         auto mk = [&](uint32_t x, uint32_t vm) { return kMasked ? (x & vm) : x; };
                         if constexpr (FP8) {
 #pragma unroll
                             for (int j2 = 0; j2 < 2; ++j2) {
                                 uint32_t R0, R1, R2, R3;
-                                ldsm_x4_t(vt + swz<true>((mi & 1) * 8 + lr, 2 * j2 + (mi >> 1)), R0, R1, R2, R3);
+                                ldsm_x4_t(vt[i] + swz<true>((mi & 1) * 8 + lr, 2 * j2 + (mi >> 1)), R0, R1, R2, R3);
                                 // rows of m-tile 2*j2 (+1): row r <-> dim 16ch + 2r, row r+8 <-> 16ch + 2r + 1;
                                 // byte pairs (0, 2) and (1, 3) of each word, gathered by one permute
                                 uint32_t v0l, v0h, v1l, v1h, v2l, v2h, v3l, v3h;
@@ -397,26 +451,45 @@ __global__ void __launch_bounds__(kThreads, TPW == 1 ? 4 : 3) decode_kernel(cons
                                 e4m3x4_to_f16x2x2(prmt(R1, 0x3120u), v1l, v1h);
                                 e4m3x4_to_f16x2x2(prmt(R2, 0x3120u), v2l, v2h);
                                 e4m3x4_to_f16x2x2(prmt(R3, 0x3120u), v3l, v3h);
-                                mma_f16(oo[2 * j2], mk(v0l, vm01), mk(v0h, vm01), mk(v1l, vm23), mk(v1h, vm23), pb0,
-                                        pb1);
-                                mma_f16(oo[2 * j2 + 1], mk(v2l, vm01), mk(v2h, vm01), mk(v3l, vm23), mk(v3h, vm23),
-                                        pb0, pb1);
+                                mma_f16(oo[2 * j2], mk(v0l, vm01[i]), mk(v0h, vm01[i]), mk(v1l, vm23[i]),
+                                        mk(v1h, vm23[i]), pb[i][0], pb[i][1]);
+                                mma_f16(oo[2 * j2 + 1], mk(v2l, vm01[i]), mk(v2h, vm01[i]), mk(v3l, vm23[i]),
+                                        mk(v3h, vm23[i]), pb[i][0], pb[i][1]);
                             }
                         } else {
 #pragma unroll
                             for (int mt = 0; mt < 4; ++mt) {
                                 uint32_t a0, a1, a2, a3;
-                                ldsm_x4_t(vt + swz<false>((mi >> 1) * 8 + lr, 2 * mt + (mi & 1)), a0, a1, a2, a3);
-                                mma_bf16(oo[mt], mk(a0, vm01), mk(a1, vm01), mk(a2, vm23), mk(a3, vm23), pb0, pb1);
+                                ldsm_x4_t(vt[i] + swz<false>((mi >> 1) * 8 + lr, 2 * mt + (mi & 1)), a0, a1, a2, a3);
+                                mma_bf16(oo[mt], mk(a0, vm01[i]), mk(a1, vm01[i]), mk(a2, vm23[i]), mk(a3, vm23[i]),
+                                         pb[i][0], pb[i][1]);
                             }
                         }
-                    };
-                    if (edge)
-                        pv(std::true_type{});
-                    else
-                        pv(std::false_type{});
-                }
+                    }
+                };
+                if (edge)
+                    pv(std::true_type{});
+                else
+                    pv(std::false_type{});
             }
+        };
+        for (int st = 0; st < nstages; ++st) {
+            const int buf = st % kStages;
+            if (!mbar_wait(&sm.full[buf], (st / kStages) & 1, p.status))
+                break;
+            const int nt = min(kConsumerWarps, ntiles - st * kConsumerWarps);  // tiles of this stage
+            int j = rep_idx;
+            if constexpr (kJoint) {
+                // the warp's tiles of the stage: four at once, else in pairs
+                if (rep == 1 && nt == kConsumerWarps) {
+                    run_tiles(std::integral_constant<int, 4>{}, buf, st, 0, 1);
+                    j = nt;
+                }
+                for (; j + rep < nt; j += 2 * rep)
+                    run_tiles(std::integral_constant<int, 2>{}, buf, st, j, rep);
+            }
+            for (; j < nt; j += rep)
+                run_tiles(std::integral_constant<int, 1>{}, buf, st, j, rep);
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(&sm.empty[buf]);
@@ -431,7 +504,7 @@ __global__ void __launch_bounds__(kThreads, TPW == 1 ? 4 : 3) decode_kernel(cons
             }
     }
     __syncthreads();  // every warp is done with the tiles: their K area holds the merge scratch
-    float *red_o = reinterpret_cast<float *>(&sm.k[0][0][0]);  // [warp][slot][dim][head]
+    float *red_o = reinterpret_cast<float *>(&sm.k[0][0][0]);  // [warp][slot][head][kRedStride]
     if (warp < kConsumerWarps) {
 #pragma unroll
         for (int tt = 0; tt < TPW; ++tt) {
@@ -441,15 +514,16 @@ __global__ void __launch_bounds__(kThreads, TPW == 1 ? 4 : 3) decode_kernel(cons
                 sm.red_l[warp][tt][2 * c] = l[tt][0];
                 sm.red_l[warp][tt][2 * c + 1] = l[tt][1];
             }
-            float *w = red_o + (warp * TPW + tt) * kHeadDim * kMaxGroup;
+            float *w0 = red_o + ((warp * TPW + tt) * kMaxGroup + 2 * c) * kRedStride;  // head 2c
+            float *w1 = w0 + kRedStride;                                                // head 2c + 1
 #pragma unroll
             for (int mt = 0; mt < 4; ++mt) {
                 const int dlo = FP8 ? 16 * mt + 2 * r : 16 * mt + r;
                 const int dhi = FP8 ? dlo + 1 : dlo + 8;
-                w[dlo * kMaxGroup + 2 * c] = o[tt][mt][0];
-                w[dlo * kMaxGroup + 2 * c + 1] = o[tt][mt][1];
-                w[dhi * kMaxGroup + 2 * c] = o[tt][mt][2];
-                w[dhi * kMaxGroup + 2 * c + 1] = o[tt][mt][3];
+                w0[dlo] = o[tt][mt][0];
+                w1[dlo] = o[tt][mt][1];
+                w0[dhi] = o[tt][mt][2];
+                w1[dhi] = o[tt][mt][3];
             }
         }
     }
@@ -472,10 +546,12 @@ __global__ void __launch_bounds__(kThreads, TPW == 1 ? 4 : 3) decode_kernel(cons
                 for (int w = w0; w < kConsumerWarps; w += wstep) {
                     const float sc = ex2(sm.red_m[w][tt][n] - M);
                     Ls += sc * sm.red_l[w][tt][n];
-                    const float *src = red_o + ((w * TPW + tt) * kHeadDim + d0) * kMaxGroup + n;
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        acc[i] += sc * src[i * kMaxGroup];
+                    const float4 src =
+                        *reinterpret_cast<const float4 *>(red_o + ((w * TPW + tt) * kMaxGroup + n) * kRedStride + d0);
+                    acc[0] += sc * src.x;
+                    acc[1] += sc * src.y;
+                    acc[2] += sc * src.z;
+                    acc[3] += sc * src.w;
                 }
             }
             const float inv = Ls > 0.f ? p.out_scale / Ls : 0.f;
@@ -510,7 +586,7 @@ size_t decode_smem_bytes()
     return sizeof(DecodeSmem<FP8, kStages>) + 1024;  // + slack for the 1 KB alignment
 }
 
-template <bool FP8, int kStages, int TPW>
+template <bool FP8, int kStages, int TPW, bool kJoint>
 cudaError_t prepare_decode()
 {
     // one cudaFuncSetAttribute per device and variant
@@ -521,7 +597,7 @@ cudaError_t prepare_decode()
         return e;
     if (dev >= 0 && dev < 64 && done[dev])
         return cudaSuccess;
-    e = cudaFuncSetAttribute(decode_kernel<FP8, kStages, TPW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(decode_kernel<FP8, kStages, TPW, kJoint>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(decode_smem_bytes<FP8, kStages>()));
     if (e == cudaSuccess && dev >= 0 && dev < 64)
         done[dev] = 1;
@@ -531,21 +607,21 @@ cudaError_t prepare_decode()
 template <bool FP8, int kStages>
 cudaError_t occupancy_of(int *blocks_per_sm)
 {
-    cudaError_t e = prepare_decode<FP8, kStages, 1>();
+    cudaError_t e = prepare_decode<FP8, kStages, 1, false>();
     if (e != cudaSuccess)
         return e;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, decode_kernel<FP8, kStages, 1>, kThreads,
-                                                         decode_smem_bytes<FP8, kStages>());
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, decode_kernel<FP8, kStages, 1, false>,
+                                                         kThreads, decode_smem_bytes<FP8, kStages>());
 }
 
-template <bool FP8, int kStages, int TPW>
+template <bool FP8, int kStages, int TPW, bool kJoint>
 cudaError_t launch_of(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p, cudaStream_t stream)
 {
-    cudaError_t e = prepare_decode<FP8, kStages, TPW>();
+    cudaError_t e = prepare_decode<FP8, kStages, TPW, kJoint>();
     if (e != cudaSuccess)
         return e;
     const dim3 grid(p.num_splits, p.num_kv_heads, p.batch);
-    decode_kernel<FP8, kStages, TPW><<<grid, kThreads, decode_smem_bytes<FP8, kStages>(), stream>>>(tk, tv, p);
+    decode_kernel<FP8, kStages, TPW, kJoint><<<grid, kThreads, decode_smem_bytes<FP8, kStages>(), stream>>>(tk, tv, p);
     return cudaGetLastError();
 }
 
@@ -562,12 +638,13 @@ cudaError_t launch_decode(const CUtensorMap &tk, const CUtensorMap &tv, const De
 {
     // two tokens per consumer warp past four tokens (measured: for q_len 2..4
     // the fourth block per SM that one token per warp allows is worth more than
-    // the second chain)
+    // the second chain); 2..4 tokens take a warp's tiles of a stage together
+    constexpr int S = kDefaultStages;
     if (p.q_len > 4)
-        return fp8 ? launch_of<true, 2 * kDefaultStages, 2>(tk, tv, p, stream)
-                   : launch_of<false, kDefaultStages, 2>(tk, tv, p, stream);
-    return fp8 ? launch_of<true, 2 * kDefaultStages, 1>(tk, tv, p, stream)
-               : launch_of<false, kDefaultStages, 1>(tk, tv, p, stream);
+        return fp8 ? launch_of<true, 2 * S, 2, false>(tk, tv, p, stream) : launch_of<false, S, 2, false>(tk, tv, p, stream);
+    if (p.q_len > 1)
+        return fp8 ? launch_of<true, 2 * S, 1, true>(tk, tv, p, stream) : launch_of<false, S, 1, true>(tk, tv, p, stream);
+    return fp8 ? launch_of<true, 2 * S, 1, false>(tk, tv, p, stream) : launch_of<false, S, 1, false>(tk, tv, p, stream);
 }
 
 }  // namespace sa
