@@ -12,12 +12,14 @@
 //                128..191  S_1 / P_1       192..255  O_1
 //
 // Warp roles (320 threads):
-//   warp 0      producer: Q tiles once, then K and V tiles (page-table walk, TMA)
+//   warp 0      producer: Q tiles once, then K and V tiles (page-table walk, TMA;
+//               for an FP8 cache the E4M3 codes, into a staging area)
 //   warp 1      MMA issuer: S_t = Q_t K^T (SS form), O_t += P_t V (P from TMEM, TS form);
 //               also zeroes the rows of the last V tile that lie past the sequence
 //   warps 2-5   softmax of head 0, warps 6-9 softmax of head 1: one thread per query
 //               row; warp w reads TMEM lanes 32*(w%4) .. +31, so each group of four
-//               warps covers all 128 rows
+//               warps covers all 128 rows.  For an FP8 cache they also widen the
+//               staged codes to f16, two tiles ahead.
 //
 // Two blocks per SM give four independent softmax streams per SM, and one
 // block's prologue, tail and epilogue overlap the other block's work.  Per key
@@ -37,10 +39,12 @@
 // are applied only on tiles that straddle a boundary.
 //
 // FP8-E4M3 caches (vLLM "GPT-OSS optimisations on NVIDIA Blackwell", FP8 KV
-// cache): TMA brings each key tile's E4M3 codes into a 4-slot staging area,
-// and the producer warp widens them (cvt e4m3x2 -> f16x2, exact for every
-// code) into the same f16 tiles (128-byte swizzle) the MMAs read, zeroing
-// rows past the sequence end.  The softmax warps convert their Q tile from
+// cache): TMA brings each key tile's E4M3 codes into a 3-slot staging area.
+// The softmax warps, right after handing over P of tile j, widen tile j + 2
+// (cvt e4m3x2 -> f16x2, exact for every code) into the 3-stage ring of f16
+// tiles (128-byte swizzle) the MMAs read, zeroing rows past the sequence end;
+// each of the 4 x NH warps takes an equal share, so the widening is spread
+// over all four SM sub-partitions instead of loading the producer's.  The softmax warps convert their Q tile from
 // bf16 to f16 in place once, P is stored as f16, the products run as
 // kind::f16 with f16 operands, and k_scale (resp. v_scale) is folded into the
 // score scale (resp. the output scale).
@@ -82,8 +86,8 @@ constexpr uint32_t kIdescPV = idesc_f32acc(BM, kHeadDim, 1, FP8);
 
 template <bool FP8>
 struct PrefillSmem {
-    static constexpr int kStages = FP8 ? 2 : 4;  // 16-bit K/V ring
-    static constexpr int kStaged = FP8 ? 4 : 1;  // FP8: slots of E4M3 codes in flight
+    static constexpr int kStages = FP8 ? 3 : 4;  // 16-bit K/V ring (FP8: widened two tiles ahead)
+    static constexpr int kStaged = FP8 ? 3 : 1;  // FP8: slots of E4M3 codes in flight
     uint8_t q[2][kQTileBytes];
     uint8_t k[kStages][kKVTileBytes];
     uint8_t v[kStages][kKVTileBytes];
@@ -93,6 +97,7 @@ struct PrefillSmem {
     uint64_t q_conv;  // FP8: Q converted to f16
     uint64_t st_full[kStaged];
     uint64_t k8_empty[kStaged];  // Q8: the QK products that read a staging slot have completed
+    uint64_t st_empty[kStaged];  // FP8: the softmax warps have widened the slot's codes
     uint64_t k_full[kStages];
     uint64_t v_full[kStages];
     uint64_t kv_empty[kStages];
@@ -113,11 +118,12 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t x)
 // One key tile of E4M3 codes (64 rows of 64 bytes as TMA wrote them with the
 // 64-byte swizzle: 16-byte chunk c of row r at chunk c ^ ((r >> 1) & 3)) ->
 // f16 values in the 128-byte-swizzled layout of a 16-bit tile (chunk c of row
-// r at chunk c ^ (r & 7)).  Rows at or past `valid` become zeros.
-__device__ __forceinline__ void widen_tile(const uint8_t *src, uint8_t *dst, int valid, int lane)
+// r at chunk c ^ (r & 7)).  Rows at or past `valid` become zeros.  Thread
+// `tid` of `nthr` takes the 16-byte chunks tid, tid + nthr, ..
+__device__ __forceinline__ void widen_tile(const uint8_t *src, uint8_t *dst, int valid, int tid, int nthr)
 {
-#pragma unroll 4
-    for (int i = lane; i < BN * 4; i += 32) {
+#pragma unroll 1
+    for (int i = tid; i < BN * 4; i += nthr) {
         const int r = i >> 2, c = i & 3;
         uint4 w = make_uint4(0u, 0u, 0u, 0u);
         if (r < valid)
@@ -284,10 +290,12 @@ __global__ void __launch_bounds__(kThreads, 2)
         for (int i = 0; i < PrefillSmem<FP8>::kStaged; ++i) {
             mbar_init(&sm.st_full[i], 1);
             mbar_init(&sm.k8_empty[i], 1);
+            mbar_init(&sm.st_empty[i], 4 * NH);
         }
         for (int i = 0; i < kStages; ++i) {
-            mbar_init(&sm.k_full[i], 1);
-            mbar_init(&sm.v_full[i], 1);
+            // FP8: every softmax warp arrives after widening its share
+            mbar_init(&sm.k_full[i], FP8 ? 4 * NH : 1);
+            mbar_init(&sm.v_full[i], FP8 ? 4 * NH : 1);
             mbar_init(&sm.kv_empty[i], 1);
         }
         for (int t = 0; t < 2; ++t) {
@@ -325,12 +333,18 @@ __global__ void __launch_bounds__(kThreads, 2)
             return trow ? __ldg(trow + key / p.page_size) : b;
         };
         if constexpr (FP8) {
-            // codes of tile j -> staging slot j % kStaged, up to kStaged tiles
-            // ahead; a slot is reused only after this warp widened (and
-            // proxy-fenced) the tile it held
+            // codes of tile j -> staging slot j % kStaged; a slot is reused once
+            // the softmax warps have widened (and proxy-fenced) the tile it held
+            // and, Q8, the QK products that read its key codes have completed
             constexpr int kStaged = PrefillSmem<FP8>::kStaged;
-            auto stage_codes = [&](int j) {
+            for (int j = 0; j < ntiles; ++j) {
                 const int sb = j % kStaged;
+                if (j >= kStaged) {
+                    const uint32_t ph = ((j / kStaged) - 1) & 1;
+                    if (!mbar_wait(&sm.st_empty[sb], ph, p.status) ||
+                        (Q8 && !mbar_wait(&sm.k8_empty[sb], ph, p.status)))
+                        break;
+                }
                 const int nbox = boxes(j);
                 const int page = page_of(j);
                 const int key = (j_first + j) * BN + 16 * lane;
@@ -346,33 +360,6 @@ __global__ void __launch_bounds__(kThreads, 2)
                 if (lane < nbox) {
                     tma_load_4d(sm.k8[sb] + lane * kBox8Bytes, &tmk, &sm.st_full[sb], 0, c1, c2, c3);
                     tma_load_4d(sm.v8[sb] + lane * kBox8Bytes, &tmv, &sm.st_full[sb], 0, c1, c2, c3);
-                }
-            };
-            int issued = 0;
-            for (int it = 0; it < ntiles; ++it) {
-                const int stage = it % kStages;
-                for (; issued < ntiles && issued < it + kStaged; ++issued) {
-                    // Q8: the slot's previous tile must have been read by its QK products
-                    if (Q8 && issued >= kStaged &&
-                        !mbar_wait(&sm.k8_empty[issued % kStaged], ((issued / kStaged) - 1) & 1, p.status))
-                        break;
-                    stage_codes(issued);
-                }
-                const int sb = it % kStaged;
-                if (!mbar_wait(&sm.st_full[sb], (it / kStaged) & 1, p.status))
-                    break;
-                if (it >= kStages && !mbar_wait(&sm.kv_empty[stage], ((it / kStages) - 1) & 1, p.status))
-                    break;
-                const int valid = min(BN, Lkv - (j_first + it) * BN);
-                if (!Q8)  // (Q8: the QK products read the key codes where TMA put them)
-                    widen_tile(sm.k8[sb], sm.k[stage], valid, lane);
-                widen_tile(sm.v8[sb], sm.v[stage], valid, lane);
-                fence_proxy_async_smem();  // generic writes -> tensor-core reads; staging reads -> next TMA
-                __syncwarp();
-                if (lane == 0) {
-                    if (!Q8)
-                        mbar_arrive(&sm.k_full[stage]);
-                    mbar_arrive(&sm.v_full[stage]);
                 }
             }
         } else {
@@ -543,6 +530,34 @@ __global__ void __launch_bounds__(kThreads, 2)
                     mbar_arrive(&sm.q_conv);
             }
         }
+        // FP8: widen the staged codes of tile j (K unless Q8, and V) into ring
+        // stage j % kStages, this thread's share of the block's softmax threads
+        auto widen = [&](int j) -> bool {
+            constexpr int kStaged = PrefillSmem<FP8>::kStaged;
+            const int sb = j % kStaged, stage = j % kStages;
+            if (!mbar_wait(&sm.st_full[sb], (j / kStaged) & 1, p.status))
+                return false;
+            // the stage's previous tile (j - kStages): its products have completed
+            if (j >= kStages && !mbar_wait(&sm.kv_empty[stage], ((j / kStages) - 1) & 1, p.status))
+                return false;
+            const int valid = min(BN, Lkv - (j_first + j) * BN);
+            const int wtid = static_cast<int>(threadIdx.x) - 32 * kFirstSoftmaxWarp;
+            if (!Q8)  // (Q8: the QK products read the key codes where TMA put them)
+                widen_tile(sm.k8[sb], sm.k[stage], valid, wtid, 128 * NH);
+            widen_tile(sm.v8[sb], sm.v[stage], valid, wtid, 128 * NH);
+            fence_proxy_async_smem();  // generic writes -> tensor-core reads; staging reads -> next TMA
+            __syncwarp();
+            if (lane == 0) {
+                if (!Q8)
+                    mbar_arrive(&sm.k_full[stage]);
+                mbar_arrive(&sm.v_full[stage]);
+                mbar_arrive(&sm.st_empty[sb]);
+            }
+            return true;
+        };
+        if constexpr (FP8)
+            for (int j = 0; ok && j < min(ntiles, kStages - 1); ++j)
+                ok = widen(j);
         for (int it = 0; ok && it < ntiles; ++it) {
             if (!mbar_wait(&sm.s_full[t], it & 1, p.status)) {
                 ok = false;
@@ -560,6 +575,9 @@ __global__ void __launch_bounds__(kThreads, 2)
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(&sm.p_full[t]);
+            if constexpr (FP8)  // the tile two ahead, while the tensor pipe runs PV and the next QK
+                if (it + kStages - 1 < ntiles)
+                    ok = widen(it + kStages - 1);
         }
         // ---- epilogue: O / l, lse = (m + log2 l) ln 2 ----
         if (ok && mbar_wait(&sm.o_done[t], 0, p.status)) {
