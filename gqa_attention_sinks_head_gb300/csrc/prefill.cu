@@ -148,21 +148,25 @@ __device__ __forceinline__ void kv_coords(const PrefillParams &p, int slot, int 
 
 // Edge tiles (straddling the causal diagonal, the window's lower edge or the
 // sequence end): overwrite the hidden keys' scores in TMEM with -inf, by
-// select, so that NaN scores past the sequence vanish too.  Interior tiles
-// skip this and the softmax body carries no mask arithmetic.
-__device__ __forceinline__ void mask_tile(uint32_t s_addr, int key0, int pos, int Lkv, int window)
+// select, so that NaN scores past the sequence vanish too.  The row sees the
+// tile's columns lo .. hi (none when hi < lo).  A 32-column chunk that every
+// row of the warp sees whole is skipped.  Interior tiles skip this and the
+// softmax body carries no mask arithmetic.
+__device__ __forceinline__ void mask_tile(uint32_t s_addr, int lo, int hi)
 {
+    // column e is visible iff (unsigned)(e - lo) <= span
+    const uint32_t span = hi >= lo ? static_cast<uint32_t>(hi - lo) : 0u;
+    const int lo_eff = hi >= lo ? lo : (1 << 20);
 #pragma unroll 1
     for (int c = 0; c < BN / 32; ++c) {
+        if (__all_sync(0xffffffffu, lo <= 32 * c && hi >= 32 * c + 31))
+            continue;
         uint32_t v[32];
         tmem_ld32(s_addr + 32 * c, v);
         tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const int key = key0 + 32 * c + i;
-            const bool vis = key <= pos && key < Lkv && (window <= 0 || key > pos - window);
-            v[i] = vis ? v[i] : 0xff800000u;
-        }
+        for (int i = 0; i < 32; ++i)
+            v[i] = static_cast<uint32_t>(32 * c + i - lo_eff) <= span ? v[i] : 0xff800000u;
         tmem_st32(s_addr + 32 * c, v);
     }
     tmem_st_wait();
@@ -567,8 +571,8 @@ __global__ void __launch_bounds__(kThreads, 2)
             const int key0 = (j_first + it) * BN;
             const bool edge =
                 key0 + BN - 1 > p_first || (p.window > 0 && key0 <= p_last - p.window) || key0 + BN > Lkv;
-            if (edge)
-                mask_tile(s_addr, key0, pos, Lkv, p.window);
+            if (edge)  // this row sees keys max(pos - window + 1, 0) .. min(pos, Lkv - 1)
+                mask_tile(s_addr, (p.window > 0 ? max(pos - p.window + 1, 0) : 0) - key0, min(pos, Lkv - 1) - key0);
             softmax_tile<FP8>(s_addr, o_addr, p.score_scale, it > 0, m, l);  // (P in f16 for both FP8 modes)
             tmem_st_wait();
             tc_fence_before();
