@@ -743,10 +743,17 @@ def run_native(args, world, rank, local):
             wl.step(stream)
     torch.cuda.synchronize()
     # Inputs smaller than twice the L2 (129 MB) are evicted before every step
-    # by a 256 MB write outside the step's events.
-    flush_buf = None
+    # by a 256 MB write outside the step's events, followed by a 256 MB read
+    # of a second buffer: the read evicts the write's dirty lines, so their
+    # write-back to DRAM happens before the step and not inside it.
+    flush_buf = flush = None
     if wl.resident_bytes() < L2_FLUSH_BYTES:
         flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+        flush_rd = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.int32, device="cuda")
+
+        def flush():
+            flush_buf.zero_()
+            flush_rd.sum()
     ci, kname, kbytes = wl.dominant()
     # The step is a short list of launch segments (a kernel, or a call); events
     # between the segments time the step and its dominant kernel on the
@@ -771,8 +778,8 @@ def run_native(args, world, rank, local):
         sampler.begin()
     with torch.cuda.stream(stream):
         for i in range(steps):
-            if flush_buf is not None:
-                flush_buf.zero_()
+            if flush is not None:
+                flush()
             evs[i][0].record(stream)
             for j, run in enumerate(runs):
                 run()
@@ -799,8 +806,7 @@ def run_native(args, world, rank, local):
         bound, nominal = "tensor", 2250.0
     traffic = ncu_traffic(kname, "config%d" % cfg)
 
-    e2e_ms, h2d, d2h = wl.e2e(stream, max(3, min(steps, 200)), 3,
-                              None if flush_buf is None else flush_buf.zero_)
+    e2e_ms, h2d, d2h = wl.e2e(stream, max(3, min(steps, 200)), 3, flush)
     e2e_value = wl.amount() * world / (e2e_ms / 1e3)
 
     line = {
@@ -811,7 +817,8 @@ def run_native(args, world, rank, local):
         "config": {"workload": workload_name(cfg), "global_batch": wl.B * world, "seq_len_max": wl.maxlen,
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "splits": [cl.get("S", 1) for cl in wl.calls],
-                   "l2": ("flushed before every step (256 MB write, outside the step's events)"
+                   "l2": ("flushed before every step (256 MB write, then a 256 MB read of another buffer so "
+                          "that no dirty line is left to write back; outside the step's events)"
                           if flush_buf is not None else
                           "inputs larger than twice the L2 (%.2f GB per step); no flush" % (wl.resident_bytes() / 1e9)),
                    "launch": "each launch segment of the step captured as a CUDA graph and replayed"
