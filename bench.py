@@ -193,6 +193,38 @@ def timed_loop(torch, stream, one, steps, warmup, flush=None):
     return sum(e0.elapsed_time(e1) for e0, e1 in evs) / steps
 
 
+class Packed:
+    """Tensors of one step laid out back to back (256-byte aligned) in one
+    device buffer with a pinned host mirror, so that one copy moves them all:
+    h2d() before the step's calls for its inputs, d2h() after them for its
+    results.  `dev` / `host` are views shaped like the given tensors, which
+    fill both sides at construction."""
+
+    def __init__(self, torch, tensors):
+        offs, end = [], 0
+        for t in tensors:
+            offs.append(end)
+            end = (end + t.numel() * t.element_size() + 255) // 256 * 256
+        self.nbytes = offs[-1] + tensors[-1].numel() * tensors[-1].element_size()  # bytes one copy moves
+        self._dev = torch.empty(max(end, 256), dtype=torch.uint8, device="cuda")
+        self._host = torch.empty(max(end, 256), dtype=torch.uint8, pin_memory=True)
+        self.dev, self.host = [], []
+        for t, o in zip(tensors, offs):
+            n = t.numel() * t.element_size()
+            dv = self._dev[o:o + n].view(t.dtype).view(t.shape)
+            hv = self._host[o:o + n].view(t.dtype).view(t.shape)
+            dv.copy_(t)
+            hv.copy_(t.cpu())
+            self.dev.append(dv)
+            self.host.append(hv)
+
+    def h2d(self):
+        self._dev[:self.nbytes].copy_(self._host[:self.nbytes], non_blocking=True)
+
+    def d2h(self):
+        self._host[:self.nbytes].copy_(self._dev[:self.nbytes], non_blocking=True)
+
+
 # --------------------------------------------------------------- workloads
 def decode_bytes(seqlens, window, hkv, hq, dim, elem_bytes, with_lse=True):
     """Algorithmic HBM bytes of one decode call: every visible K and V element
@@ -334,31 +366,27 @@ class DecodeBench:
 
     # ---- end to end through sa_decode with host buffers
     def e2e(self, stream, steps, warmup, flush=None):
+        """Per step: one copy of q, the sequence lengths and the page table in,
+        the calls, one copy of every call's out and lse back."""
+        import dataclasses
         torch = self.torch
         c = self.case
-        hq = torch.empty(c.q.shape, dtype=c.q.dtype, pin_memory=True).copy_(c.q.cpu())
-        hs = torch.empty(c.seqlens.shape, dtype=torch.int32, pin_memory=True).copy_(c.seqlens.cpu())
-        ht = None
-        if c.kv.page_table is not None:
-            ht = torch.empty(c.kv.page_table.shape, dtype=torch.int32, pin_memory=True).copy_(c.kv.page_table.cpu())
-        houts = [(torch.empty(cl["out"].shape, dtype=torch.bfloat16, pin_memory=True),
-                  torch.empty(cl["lse"].shape, dtype=torch.float32, pin_memory=True)) for cl in self.calls]
-        h2d = hq.numel() * 2 + hs.numel() * 4 + (0 if ht is None else ht.numel() * 4)
-        d2h = sum(o.numel() * 2 + l.numel() * 4 for o, l in houts)
+        paged = c.kv.page_table is not None
+        inp = Packed(torch, [c.q, c.seqlens] + ([c.kv.page_table] if paged else []))
+        q, seqlens = inp.dev[0], inp.dev[1]
+        kv = dataclasses.replace(c.kv, page_table=inp.dev[2]) if paged else c.kv
+        res = Packed(torch, [t for cl in self.calls for t in (cl["out"], cl["lse"])])
 
         def one():
-            c.q.copy_(hq, non_blocking=True)
-            c.seqlens.copy_(hs, non_blocking=True)
-            if ht is not None:
-                c.kv.page_table.copy_(ht, non_blocking=True)
-            for cl, (ho, hl) in zip(self.calls, houts):
-                self.sa.sa_decode(c.q, c.kv, c.seqlens, c.sinks, cl["window"], c.sm_scale, cl["out"], cl["lse"],
-                                  max_kv_len=self.maxlen, workspace=cl["ws"], num_splits=cl["S"], stream=stream)
-                ho.copy_(cl["out"], non_blocking=True)
-                hl.copy_(cl["lse"], non_blocking=True)
+            inp.h2d()
+            for i, cl in enumerate(self.calls):
+                self.sa.sa_decode(q, kv, seqlens, c.sinks, cl["window"], c.sm_scale, res.dev[2 * i],
+                                  res.dev[2 * i + 1], max_kv_len=self.maxlen, workspace=cl["ws"], num_splits=cl["S"],
+                                  stream=stream)
+            res.d2h()
 
         ms = timed_loop(torch, stream, one, steps, warmup, flush)
-        return ms, h2d, d2h
+        return ms, inp.nbytes, res.nbytes
 
     # ---- oracle on a bounded sample
     def oracle_sample(self, budget_s, max_seqs=None):
@@ -447,27 +475,26 @@ class MultiDecodeBench:
         return [lambda cl=cl: self.run_call(cl, stream) for cl in self.calls]
 
     def e2e(self, stream, steps, warmup, flush=None):
+        """Per step: one copy of q, the sequence lengths and the page table in,
+        the calls, one copy of every call's out and lse back."""
+        import dataclasses
         torch = self.torch
         c = self.case
-        hq = torch.empty(c.q.shape, dtype=c.q.dtype, pin_memory=True).copy_(c.q.cpu())
-        hs = torch.empty(c.seqlens.shape, dtype=torch.int32, pin_memory=True).copy_(c.seqlens.cpu())
-        ht = torch.empty(c.kv.page_table.shape, dtype=torch.int32, pin_memory=True).copy_(c.kv.page_table.cpu())
-        houts = [(torch.empty(cl["out"].shape, dtype=torch.bfloat16, pin_memory=True),
-                  torch.empty(cl["lse"].shape, dtype=torch.float32, pin_memory=True)) for cl in self.calls]
-        h2d = hq.numel() * 2 + hs.numel() * 4 + ht.numel() * 4
-        d2h = sum(o.numel() * 2 + l.numel() * 4 for o, l in houts)
+        inp = Packed(torch, [c.q, c.seqlens, c.kv.page_table])
+        q, seqlens = inp.dev[0], inp.dev[1]
+        kv = dataclasses.replace(c.kv, page_table=inp.dev[2])
+        res = Packed(torch, [t for cl in self.calls for t in (cl["out"], cl["lse"])])
 
         def one():
-            c.q.copy_(hq, non_blocking=True)
-            c.seqlens.copy_(hs, non_blocking=True)
-            c.kv.page_table.copy_(ht, non_blocking=True)
-            for cl, (ho, hl) in zip(self.calls, houts):
-                self.run_call(cl, stream)
-                ho.copy_(cl["out"], non_blocking=True)
-                hl.copy_(cl["lse"], non_blocking=True)
+            inp.h2d()
+            for i, cl in enumerate(self.calls):
+                self.sa.sa_decode_multi(q, self.q_len, kv, seqlens, c.sinks, cl["window"], c.sm_scale,
+                                        res.dev[2 * i], res.dev[2 * i + 1], max_kv_len=self.maxlen,
+                                        workspace=cl["ws"], num_splits=cl["S"], stream=stream)
+            res.d2h()
 
         ms = timed_loop(torch, stream, one, steps, warmup, flush)
-        return ms, h2d, d2h
+        return ms, inp.nbytes, res.nbytes
 
     def oracle_sample(self, budget_s, max_seqs=None):
         """Every token row of the first n sequences, all heads, every call."""
@@ -553,21 +580,20 @@ class RopeBench:
         return [lambda cl=cl: self.run_call(cl, stream) for cl in self.calls]
 
     def e2e(self, stream, steps, warmup, flush=None):
+        """Per step: one copy of q, k, v and the positions in, the call, the
+        rotated q back; the cache stays resident."""
         torch = self.torch
-        hs = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t.cpu()) for t in
-              (self.q, self.k, self.v, self.pos)]
+        inp = Packed(torch, [self.q, self.k, self.v, self.pos])
+        q, k, v, pos = inp.dev
         hout = torch.empty(self.q_out.shape, dtype=torch.bfloat16, pin_memory=True)
-        h2d = sum(t.numel() * t.element_size() for t in hs)
-        d2h = hout.numel() * 2
 
         def one():
-            for dev, host in zip((self.q, self.k, self.v, self.pos), hs):
-                dev.copy_(host, non_blocking=True)
-            self.run_call(self.calls[0], stream)
+            inp.h2d()
+            self.sa.sa_rope_append(q, k, v, self.seq, pos, self.table, self.kv, 1, self.q_out, stream=stream)
             hout.copy_(self.q_out, non_blocking=True)
 
         ms = timed_loop(torch, stream, one, steps, warmup, flush)
-        return ms, h2d, d2h
+        return ms, inp.nbytes, hout.numel() * 2
 
     def oracle_sample(self, budget_s, max_seqs=None):
         """The oracle's rotation + cache write of the first n tokens."""
@@ -647,17 +673,21 @@ class PrefillBench:
         q = self.q_codes if self.q8 else c.q
         return q.numel() * q.element_size() + (c.kv.k.numel() + c.kv.v.numel()) * c.kv.k.element_size()
 
-    def run_call(self, cl, stream, ev=None):
+    def run_call(self, cl, stream, ev=None, q=None, kv=None, out=None, lse=None):
         c = self.case
+        kv = c.kv if kv is None else kv
+        out = cl["out"] if out is None else out
+        lse = cl["lse"] if lse is None else lse
         if ev is not None:
             ev[0].record(stream)
         if self.q8:
-            self.sa.sa_prefill_q8(self.q_codes, self.q_scale, c.cu_seqlens_q, c.kv, c.seqlens, c.sinks, cl["window"],
-                                  c.sm_scale, cl["out"], cl["lse"], max_q_len=max(self.q_lens),
+            self.sa.sa_prefill_q8(self.q_codes if q is None else q, self.q_scale, c.cu_seqlens_q, kv, c.seqlens,
+                                  c.sinks, cl["window"], c.sm_scale, out, lse, max_q_len=max(self.q_lens),
                                   max_kv_len=self.maxlen, stream=stream)
         else:
-            self.sa.sa_prefill(c.q, c.cu_seqlens_q, c.kv, c.seqlens, c.sinks, cl["window"], c.sm_scale, cl["out"],
-                               cl["lse"], max_q_len=max(self.q_lens), max_kv_len=self.maxlen, stream=stream)
+            self.sa.sa_prefill(c.q if q is None else q, c.cu_seqlens_q, kv, c.seqlens, c.sinks, cl["window"],
+                               c.sm_scale, out, lse, max_q_len=max(self.q_lens), max_kv_len=self.maxlen,
+                               stream=stream)
         if ev is not None:
             ev[1].record(stream)
 
@@ -673,28 +703,24 @@ class PrefillBench:
         return [lambda cl=cl: self.run_call(cl, stream) for cl in self.calls]
 
     def e2e(self, stream, steps, warmup, flush=None):
+        """Per step: one copy of q (or its codes), k and v in, the calls, one
+        copy of every call's out and lse back."""
+        import dataclasses
         torch = self.torch
         c = self.case
-        qdev = self.q_codes if self.q8 else c.q
-        hq = torch.empty(qdev.shape, dtype=qdev.dtype, pin_memory=True).copy_(qdev.cpu())
-        hk = torch.empty(c.kv.k.shape, dtype=c.kv.k.dtype, pin_memory=True).copy_(c.kv.k.cpu())
-        hv = torch.empty(c.kv.v.shape, dtype=c.kv.v.dtype, pin_memory=True).copy_(c.kv.v.cpu())
-        houts = [(torch.empty(cl["out"].shape, dtype=torch.bfloat16, pin_memory=True),
-                  torch.empty(cl["lse"].shape, dtype=torch.float32, pin_memory=True)) for cl in self.calls]
-        h2d = hq.numel() * hq.element_size() + (hk.numel() + hv.numel()) * hk.element_size()
-        d2h = sum(o.numel() * 2 + l.numel() * 4 for o, l in houts)
+        inp = Packed(torch, [self.q_codes if self.q8 else c.q, c.kv.k, c.kv.v])
+        q = inp.dev[0]
+        kv = dataclasses.replace(c.kv, k=inp.dev[1], v=inp.dev[2])
+        res = Packed(torch, [t for cl in self.calls for t in (cl["out"], cl["lse"])])
 
         def one():
-            qdev.copy_(hq, non_blocking=True)
-            c.kv.k.copy_(hk, non_blocking=True)
-            c.kv.v.copy_(hv, non_blocking=True)
-            for cl, (ho, hl) in zip(self.calls, houts):
-                self.run_call(cl, stream)
-                ho.copy_(cl["out"], non_blocking=True)
-                hl.copy_(cl["lse"], non_blocking=True)
+            inp.h2d()
+            for i, cl in enumerate(self.calls):
+                self.run_call(cl, stream, q=q, kv=kv, out=res.dev[2 * i], lse=res.dev[2 * i + 1])
+            res.d2h()
 
         ms = timed_loop(torch, stream, one, steps, warmup, flush)
-        return ms, h2d, d2h
+        return ms, inp.nbytes, res.nbytes
 
     def oracle_sample(self, budget_s, max_seqs=None):
         """Rows of the sequence, all heads: the first, then every k-th."""
