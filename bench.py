@@ -873,6 +873,17 @@ def run_native(args, world, rank, local):
                                 "cores": getattr(wl, "oracle_cores", 0) or oracle.num_threads(), "kind": "oracle",
                                 "sample": "%s; timed %d times" % (desc, reps),
                                 "seconds": round(dt, 2)}
+        if cfg == 1:  # the smallest workload: the oracle on one thread as well
+            cores = oracle.num_threads()
+            oracle.set_num_threads(1)
+            try:
+                dt1, nb1, reps1 = 0.0, 0, 0
+                while dt1 < 3.0 and reps1 < 1000:
+                    d1, b1, _ = wl.oracle_sample(30.0)
+                    dt1, nb1, reps1 = dt1 + d1, nb1 + b1, reps1 + 1
+            finally:
+                oracle.set_num_threads(cores)
+            line["cpu_baseline"]["single_thread_value"] = round(nb1 / 1e9 / dt1, 6)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -91,12 +91,19 @@ def _load():
             lib.sao_bf16_array.argtypes = [P, ctypes.c_int64, P]
             lib.sao_e4m3_array.argtypes = [P, ctypes.c_int64, P]
             lib.sao_num_threads.restype = ctypes.c_int
+            lib.sao_set_num_threads.restype = None
+            lib.sao_set_num_threads.argtypes = [ctypes.c_int]
             _lib = lib
     return _lib
 
 
 def num_threads() -> int:
     return int(_load().sao_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """Threads of the oracle's next parallel loops (for timing; the results do not depend on it)."""
+    _load().sao_set_num_threads(int(n))
 
 
 # ---------------------------------------------------------------- marshalling

@@ -463,3 +463,14 @@ int sao_num_threads(void)
     return 1;
 #endif
 }
+
+/* Threads the next parallel loops use (timing only; results do not depend on it). */
+void sao_set_num_threads(int n)
+{
+#ifdef _OPENMP
+    if (n > 0)
+        omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}

@@ -441,3 +441,20 @@ def test_e4m3_query_with_power_of_two_scale_equals_bf16_query(oracle):
                       q_scale=0.125)
     b = oracle.attend(q_bf16, rows[0], rows[1], case.kv.as_dict(), case.seqlens, case.sinks, 0, case.sm_scale)
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_thread_count_does_not_change_results(oracle):
+    """The oracle parallelises over (row, head) pairs only; each pair is summed
+    in one fixed order, so its result is bit-identical on any thread count."""
+    case = W.make_decode_case([1, 40, 333, 1024], page_size=16, window=0, poison_pages=2, seed=77)
+    rows = oracle.decode_rows(case.seqlens)
+    cores = oracle.num_threads()
+    try:
+        outs = []
+        for n in (1, max(cores, 2)):
+            oracle.set_num_threads(n)
+            outs.append(oracle.attend(case.q, rows[0], rows[1], case.kv.as_dict(), case.seqlens, case.sinks,
+                                      0, case.sm_scale))
+    finally:
+        oracle.set_num_threads(cores)
+    assert np.array_equal(outs[0][0], outs[1][0]) and np.array_equal(outs[0][1], outs[1][1])
