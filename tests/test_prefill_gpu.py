@@ -171,3 +171,20 @@ def test_q8_config7_full_size(sa, oracle):
     sel = np.unique(np.concatenate([np.arange(0, 8192, 1024), np.arange(1023, 8192, 1024),
                                     g.choice(8192, 40, replace=False)])).astype(np.int32)
     run_q8(sa, oracle, case, "q8 config 7", sel=sel)
+
+
+@pytest.mark.parametrize("mode", ["bf16", "e4m3", "q8"])
+@pytest.mark.parametrize("window", [0, 128])
+def test_one_head_per_block_long_ragged(sa, oracle, mode, window):
+    """Odd GQA groups run one head per block (128 softmax threads, which then
+    widen an FP8 tile in two 16-byte chunks each).  Sequences long enough for
+    the staging slots and the K/V ring to wrap several times, ragged and paged."""
+    kv_dtype = "bf16" if mode == "bf16" else "e4m3"
+    case = W.make_prefill_case([700, 37, 300], [1000, 37, 1029], num_qo_heads=6, num_kv_heads=2, paged=True,
+                               page_size=16, layout="HND", window=window, kv_dtype=kv_dtype, poison_pages=4,
+                               seed=340 + window)
+    what = "one head per block, %s, w=%d" % (mode, window)
+    if mode == "q8":
+        run_q8(sa, oracle, case, what)
+    else:
+        run(sa, oracle, case, what)
