@@ -347,6 +347,28 @@ class DecodeBench:
     def dominant(self):
         return 0, "decode_kernel", self.calls[0]["bytes"]
 
+    def segment_names(self):
+        names = []
+        for cl in self.calls:
+            if cl["S"] > 1:
+                names += ["decode w=%d (%d chunks)" % (cl["window"], cl["S"]), "merge w=%d" % cl["window"]]
+            else:
+                names.append("decode w=%d" % cl["window"])
+        return names
+
+    def notes(self, seg_ms, peaks):
+        """Calls too small to stream at HBM rate are reported in microseconds."""
+        out, j = {}, 0
+        for cl in self.calls:
+            n = 2 if cl["S"] > 1 else 1
+            ms = sum(seg_ms[j:j + n])
+            j += n
+            if cl["bytes"] < 64e6:
+                out["decode w=%d" % cl["window"]] = {
+                    "us": round(ms * 1e3, 2), "GB/s": round(cl["bytes"] / 1e6 / ms, 1),
+                    "bound": "latency (one wave of short blocks; launch and one HBM round trip dominate)"}
+        return out
+
     def segments(self, stream):
         """The step as launch segments: decode kernel, then its merge when split."""
         sa, c = self.sa, self.case
@@ -470,6 +492,15 @@ class MultiDecodeBench:
     def dominant(self):
         return 0, "decode_kernel (with its merge)", self.calls[0]["bytes"]
 
+    def segment_names(self):
+        return ["decode q_len=%d w=%d (%d chunks)" % (self.q_len, cl["window"], cl["S"]) for cl in self.calls]
+
+    def notes(self, seg_ms, peaks):
+        return {"decode q_len=%d w=%d" % (self.q_len, cl["window"]): {
+                    "us": round(ms * 1e3, 2), "GB/s": round(cl["bytes"] / 1e6 / ms, 1),
+                    "bound": "latency (one wave of short blocks)"}
+                for cl, ms in zip(self.calls, seg_ms) if cl["bytes"] < 64e6}
+
     def segments(self, stream):
         """The step as launch segments: one per call."""
         return [lambda cl=cl: self.run_call(cl, stream) for cl in self.calls]
@@ -575,6 +606,9 @@ class RopeBench:
     def dominant(self):
         return 0, "rope_append_kernel", self.step_bytes
 
+    def segment_names(self):
+        return ["rope_append"]
+
     def segments(self, stream):
         """The step as launch segments: one per call."""
         return [lambda cl=cl: self.run_call(cl, stream) for cl in self.calls]
@@ -663,6 +697,14 @@ class PrefillBench:
         self.e2e_api = "sa_prefill with pinned host q, k, v in, out/lse of both calls back"
         self.B = len(self.q_lens)
         self.maxlen = max(self.kv_lens)
+        # algorithmic bytes of a call: q in, out and lse back, and the K/V rows
+        # some query of the call sees (a window call is bound by these, not by flops)
+        qe = 1 if self.q8 else 2
+        for cl in self.calls:
+            w = cl["window"]
+            keys = sum(min(L, lq + w - 1) if w > 0 else L for lq, L in zip(self.q_lens, self.kv_lens))
+            cl["bytes"] = (sum(self.q_lens) * self.Hq * (self.D * qe + self.D * 2 + 4)
+                           + keys * self.Hkv * self.D * 2 * self.elem)
 
     def amount(self):
         return self.step_flops / 1e12
@@ -697,6 +739,22 @@ class PrefillBench:
 
     def dominant(self):
         return 0, "prefill_kernel", self.calls[0]["flops"]
+
+    def segment_names(self):
+        return ["prefill w=%d" % cl["window"] for cl in self.calls]
+
+    def notes(self, seg_ms, peaks):
+        """Window calls against their HBM roofline as well as in TFLOP/s."""
+        out = {}
+        hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+        for cl, ms in zip(self.calls, seg_ms):
+            if cl["window"] > 0:
+                gbs = cl["bytes"] / 1e6 / ms
+                out["prefill w=%d" % cl["window"]] = {
+                    "us": round(ms * 1e3, 1), "TFLOP/s": round(cl["flops"] / 1e9 / ms, 1),
+                    "algorithmic_bytes": cl["bytes"], "GB/s": round(gbs, 1), "frac_of_hbm": round(gbs / hbm, 4),
+                    "hbm_floor_us": round(cl["bytes"] / hbm / 1e3, 1)}
+        return out
 
     def segments(self, stream):
         """The step as launch segments: one per call."""
@@ -815,6 +873,8 @@ def run_native(args, world, rank, local):
         sampler.end()
     dist_barrier(world)
     ms = statistics.fmean(e[0].elapsed_time(e[-1]) for e in evs)
+    ms_median = statistics.median(e[0].elapsed_time(e[-1]) for e in evs)
+    seg_ms = [statistics.fmean(e[j].elapsed_time(e[j + 1]) for e in evs) for j in range(len(runs))]
     ms = dist_max(ms, world)
     k_ms = statistics.fmean(e[ci].elapsed_time(e[ci + 1]) for e in evs)
     clocks = sampler.stop() if sampler else None
@@ -860,7 +920,15 @@ def run_native(args, world, rank, local):
         "e2e": {"value": round(e2e_value, 2), "unit": wl.unit, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "api": wl.e2e_api},
         "gpu_launches": steps * wl.kernels_per_step,  # the library's kernels (the L2 flush is torch's)
+        "ms_per_step_median": round(ms_median, 6),
+        "segments": [{"name": n, "ms": round(t, 6)} for n, t in
+                     zip(getattr(wl, "segment_names", lambda: ["segment %d" % j for j in range(len(seg_ms))])(),
+                         seg_ms)],
     }
+    if hasattr(wl, "notes"):
+        notes = wl.notes(seg_ms, peaks)
+        if notes:
+            line["notes"] = notes
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
         # repeat the sample until about 10 s of host work is timed
