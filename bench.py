@@ -855,12 +855,28 @@ def run_native(args, world, rank, local):
                 fn()
             runs.append(g.replay)
         torch.cuda.synchronize()
+    # Two passes of K steps each.  The first times whole steps, with events
+    # only at step boundaries (so that no event sits between the launches of
+    # a step): the step time and `value`.  The second repeats the steps with
+    # an event after every segment: the dominant kernel's time and the
+    # segment breakdown.
+    step_evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(runs) + 1)] for _ in range(steps)]
     dist_barrier(world)
     torch.cuda.synchronize()
     if sampler:
         sampler.begin()
-    with torch.cuda.stream(stream):
+    with torch.cuda.stream(stream):  # the timed region: K steps
+        for i in range(steps):
+            if flush is not None:
+                flush()
+            step_evs[i][0].record(stream)
+            for run in runs:
+                run()
+            step_evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    dist_barrier(world)
+    with torch.cuda.stream(stream):  # the segment breakdown: K more steps
         for i in range(steps):
             if flush is not None:
                 flush()
@@ -872,8 +888,8 @@ def run_native(args, world, rank, local):
     if sampler:
         sampler.end()
     dist_barrier(world)
-    ms = statistics.fmean(e[0].elapsed_time(e[-1]) for e in evs)
-    ms_median = statistics.median(e[0].elapsed_time(e[-1]) for e in evs)
+    ms = statistics.fmean(e[0].elapsed_time(e[1]) for e in step_evs)
+    ms_median = statistics.median(e[0].elapsed_time(e[1]) for e in step_evs)
     seg_ms = [statistics.fmean(e[j].elapsed_time(e[j + 1]) for e in evs) for j in range(len(runs))]
     ms = dist_max(ms, world)
     k_ms = statistics.fmean(e[ci].elapsed_time(e[ci + 1]) for e in evs)
@@ -909,7 +925,9 @@ def run_native(args, world, rank, local):
                           "inputs larger than twice the L2 (%.2f GB per step); no flush" % (wl.resident_bytes() / 1e9)),
                    "launch": "each launch segment of the step captured as a CUDA graph and replayed"
                              if args.graph else "eager",
-                   "timing": "CUDA events around each step on its stream; mean over the steps"},
+                   "timing": "CUDA events around each step on its stream, none between a step's launches; mean "
+                             "over the K steps. A second pass of K steps with an event after every launch segment "
+                             "times the dominant kernel and the segments."},
         "roofline": {"bound": bound, "achieved": round(achieved, 1), "peak": peak, "unit": wl.unit,
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "kernel": kname, ("algorithmic_bytes_per_launch" if bound == "hbm"
@@ -919,7 +937,7 @@ def run_native(args, world, rank, local):
         "clocks": clocks,
         "e2e": {"value": round(e2e_value, 2), "unit": wl.unit, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "api": wl.e2e_api},
-        "gpu_launches": steps * wl.kernels_per_step,  # the library's kernels (the L2 flush is torch's)
+        "gpu_launches": steps * wl.kernels_per_step,  # timed region; the library's kernels (the L2 flush is torch's)
         "ms_per_step_median": round(ms_median, 6),
         "segments": [{"name": n, "ms": round(t, 6)} for n, t in
                      zip(getattr(wl, "segment_names", lambda: ["segment %d" % j for j in range(len(seg_ms))])(),
