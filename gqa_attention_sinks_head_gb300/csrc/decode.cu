@@ -114,6 +114,10 @@ __global__ void __launch_bounds__(kThreads, TPW == 1 ? 4 : 3) decode_kernel(cons
     DecodeSmem<FP8, kStages> &sm =
         *reinterpret_cast<DecodeSmem<FP8, kStages> *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
+    // launched as a programmatic dependent: the grid before it has finished
+    // (and its writes are visible) before any global access below
+    griddep_wait();
+    griddep_launch_dependents();  // the next grid (a merge, the next call) may be scheduled
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int split = blockIdx.x;
@@ -575,9 +579,6 @@ __global__ void __launch_bounds__(kThreads, TPW == 1 ? 4 : 3) decode_kernel(cons
             }
         }
     }
-    // This block's outputs are written: a programmatically dependent grid
-    // (the merge of a split decode) may start launching.
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 template <bool FP8, int kStages>
@@ -621,8 +622,8 @@ cudaError_t launch_of(const CUtensorMap &tk, const CUtensorMap &tv, const Decode
     if (e != cudaSuccess)
         return e;
     const dim3 grid(p.num_splits, p.num_kv_heads, p.batch);
-    decode_kernel<FP8, kStages, TPW, kJoint><<<grid, kThreads, decode_smem_bytes<FP8, kStages>(), stream>>>(tk, tv, p);
-    return cudaGetLastError();
+    return launch_pdl(decode_kernel<FP8, kStages, TPW, kJoint>, grid, dim3(kThreads), decode_smem_bytes<FP8, kStages>(),
+                      stream, tk, tv, p);
 }
 
 }  // namespace

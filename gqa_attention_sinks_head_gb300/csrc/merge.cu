@@ -24,7 +24,8 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergePara
     // Launched as a programmatic dependent of the split decode: wait here until
     // that grid has finished and its partial states are visible (returns at
     // once when there is no such dependency).
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    griddep_wait();
+    griddep_launch_dependents();  // the next call's grid may be scheduled as this one drains
     const int lane = threadIdx.x & 31;
     const int64_t NH = static_cast<int64_t>(p.n) * p.num_heads;
     const int64_t row = static_cast<int64_t>(blockIdx.x) * kMergeWarps + (threadIdx.x >> 5);
@@ -105,17 +106,7 @@ cudaError_t launch_merge(const MergeParams &p, cudaStream_t stream)
     // Programmatic dependent launch: the merge grid may be scheduled while the
     // kernel before it on the stream drains; griddepcontrol.wait above orders
     // the reads.
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(blocks));
-    cfg.blockDim = dim3(kMergeWarps * 32);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, merge_kernel, p);
+    return launch_pdl(merge_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kMergeWarps * 32), 0, stream, p);
 }
 
 }  // namespace sa

@@ -255,6 +255,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     extern __shared__ uint8_t smem_raw[];
     PrefillSmem<FP8> &sm =
         *reinterpret_cast<PrefillSmem<FP8> *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // launched as a programmatic dependent: the grid before it has finished
+    // (and its writes are visible) before any global access below
+    griddep_wait();
+    griddep_launch_dependents();  // the next call's grid may be scheduled as this one drains
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int NH = p.heads_per_cta;
@@ -644,8 +648,7 @@ cudaError_t launch_of(const CUtensorMap &tq, const CUtensorMap &tk, const CUtens
             done[dev] = 1;
     }
     const dim3 grid(p.num_qo_heads / p.heads_per_cta, p.num_q_tiles, p.batch);
-    prefill_kernel<FP8, Q8><<<grid, kThreads, prefill_smem_bytes<FP8>(), stream>>>(tq, tk, tv, p);
-    return cudaGetLastError();
+    return launch_pdl(prefill_kernel<FP8, Q8>, grid, dim3(kThreads), prefill_smem_bytes<FP8>(), stream, tq, tk, tv, p);
 }
 
 }  // namespace

@@ -125,6 +125,10 @@ __device__ __forceinline__ void finish_row(const RopeParams &p, int t, int j, in
 template <bool kCacheFp8, bool kQFp8>
 __global__ void __launch_bounds__(kThreads, 4) rope_append_kernel(const RopeParams p)
 {
+    // launched as a programmatic dependent: the grid before it has finished
+    // (and its writes are visible) before any global access below
+    griddep_wait();
+    griddep_launch_dependents();
     const int sub = threadIdx.x & 3;
     const uint32_t heads = p.num_qo_heads + 2 * p.num_kv_heads;
     const uint32_t nrows = static_cast<uint32_t>(p.num_tokens) * heads;  // < 2^31 (checked on the host)
@@ -180,13 +184,9 @@ cudaError_t launch_rope_append(const RopeParams &p, cudaStream_t stream)
     if (blocks == 0)
         return cudaSuccess;
     const unsigned nb = static_cast<unsigned>(blocks);
-    if (p.fp8)
-        p.q_fp8 ? rope_append_kernel<true, true><<<nb, kThreads, 0, stream>>>(p)
-                : rope_append_kernel<true, false><<<nb, kThreads, 0, stream>>>(p);
-    else
-        p.q_fp8 ? rope_append_kernel<false, true><<<nb, kThreads, 0, stream>>>(p)
-                : rope_append_kernel<false, false><<<nb, kThreads, 0, stream>>>(p);
-    return cudaGetLastError();
+    auto kernel = p.fp8 ? (p.q_fp8 ? rope_append_kernel<true, true> : rope_append_kernel<true, false>)
+                        : (p.q_fp8 ? rope_append_kernel<false, true> : rope_append_kernel<false, false>);
+    return launch_pdl(kernel, dim3(nb), dim3(kThreads), 0, stream, p);
 }
 
 }  // namespace sa

@@ -6,6 +6,8 @@
 #include <cuda_runtime_api.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/sink_attn.h"
 
 namespace sa {
@@ -82,6 +84,26 @@ struct RopeParams {
 
 // Record `fmt` as the calling thread's sa_last_error() message and return st.
 sa_status_t set_last_error(sa_status_t st, const char *fmt, ...);
+
+// Launch `kernel` on `stream` with programmatic stream serialization: its
+// blocks may be scheduled while the kernel before it on the stream drains
+// (the kernel itself waits for that grid before any global memory access).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Launchers (return the launch error, if any).
 cudaError_t launch_decode(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p,
