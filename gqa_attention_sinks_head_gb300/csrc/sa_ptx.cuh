@@ -213,17 +213,10 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t sel)
     return d;
 }
 
-// Two E4M3 codes (the low 16 bits of w, lowest byte first) -> their values as
-// f16x2, exactly: every E4M3 value, subnormals included, is an f16 normal.
-// Codes 0x7F / 0xFF (NaN in E4M3) give f16 NaN.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t w)
-{
-    uint32_t d;
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"(static_cast<unsigned short>(w)));
-    return d;
-}
-
-// Four E4M3 codes (bytes 0..3 of w) -> two f16x2: bytes (0, 1) in lo, (2, 3) in hi.
+// Four E4M3 codes (bytes 0..3 of w) -> their values as two f16x2: bytes
+// (0, 1) in lo, (2, 3) in hi, lowest byte in the low half.  Exact: every E4M3
+// value, subnormals included, is an f16 normal; codes 0x7F / 0xFF (NaN in
+// E4M3) give f16 NaN.
 __device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t &lo, uint32_t &hi)
 {
     asm("{\n\t.reg .b16 a, b;\n\t"
@@ -268,20 +261,6 @@ __device__ __forceinline__ void tmem_relinquish()
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
 {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
-
-// Warpgroup register rebalancing: the block launches with N registers per
-// thread; warpgroups that need fewer give them back (dec) so that others can
-// grow (inc).  The sum over warpgroups must stay within the launch allocation.
-template <uint32_t N>
-__device__ __forceinline__ void regs_dec()
-{
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
-}
-template <uint32_t N>
-__device__ __forceinline__ void regs_inc()
-{
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -386,16 +365,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
         "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
         "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
         "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
-        : "memory");
-}
-
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16])
-{
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
-        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
         : "memory");
 }
 
