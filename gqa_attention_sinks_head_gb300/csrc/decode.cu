@@ -38,9 +38,9 @@
 // speculative and MTP decoders): token k of sequence b sits at position
 // L_b - q_len + k.  Each consumer warp owns one token (q_len <= 4) or two
 // (TPW = 2, q_len 5..8: two softmax chains interleaved on the same K/V
-// fragments); the warps that own the same tokens take turns over the tiles of
-// a stage.  The block still reads each K/V byte of the kv head once for all
-// tokens and heads.
+// fragments); the warps that own the same tokens split the tiles of a stage,
+// and a warp's tiles of a stage run as one block of 32 or 64 keys.  The block
+// still reads each K/V byte of the kv head once for all tokens and heads.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -97,15 +97,15 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk)
         return row * 128 + ((chunk ^ (row & 7)) << 4);
 }
 
-// kJoint: a warp that owns several tiles of a stage (2..4 query tokens) runs
-// them as one block; the one-token kernel is built without that path.
+// kJoint: a warp that owns several tiles of a stage (2..8 query tokens) runs
+// them as one block; the one-token kernel is built without that path.  With
+// two tokens per warp (TPW 2) that takes more registers: two blocks per SM.
 template <bool FP8, int kStages, int TPW, bool kJoint>
-__global__ void __launch_bounds__(kThreads, TPW == 1 ? 4 : 3) decode_kernel(const __grid_constant__ CUtensorMap tmk,
+__global__ void __launch_bounds__(kThreads, TPW == 1 ? 4 : (kJoint ? 2 : 3)) decode_kernel(const __grid_constant__ CUtensorMap tmk,
                                                                           const __grid_constant__ CUtensorMap tmv,
                                                                           const DecodeParams p)
 {
     using Cfg = DecodeCfg<FP8>;
-    static_assert(!kJoint || TPW == 1, "joint tiles are built for one token per warp");
     extern __shared__ uint8_t smem_raw[];
     // the per-warp O^T partials of the final merge reuse the K tiles
     static_assert(sizeof(float) * kConsumerWarps * TPW * kMaxGroup * kRedStride <=
@@ -639,10 +639,12 @@ cudaError_t launch_decode(const CUtensorMap &tk, const CUtensorMap &tv, const De
 {
     // two tokens per consumer warp past four tokens (measured: for q_len 2..4
     // the fourth block per SM that one token per warp allows is worth more than
-    // the second chain); 2..4 tokens take a warp's tiles of a stage together
+    // the second chain); from 2 tokens on, a warp takes its tiles of a stage
+    // together (q_len 5..8: 2 blocks per SM, 10-12 % over one tile at a time
+    // at 3 blocks per SM)
     constexpr int S = kDefaultStages;
     if (p.q_len > 4)
-        return fp8 ? launch_of<true, 2 * S, 2, false>(tk, tv, p, stream) : launch_of<false, S, 2, false>(tk, tv, p, stream);
+        return fp8 ? launch_of<true, 2 * S, 2, true>(tk, tv, p, stream) : launch_of<false, S, 2, true>(tk, tv, p, stream);
     if (p.q_len > 1)
         return fp8 ? launch_of<true, 2 * S, 1, true>(tk, tv, p, stream) : launch_of<false, S, 1, true>(tk, tv, p, stream);
     return fp8 ? launch_of<true, 2 * S, 1, false>(tk, tv, p, stream) : launch_of<false, S, 1, false>(tk, tv, p, stream);
