@@ -692,8 +692,10 @@ class PrefillBench:
         self.unit = "TFLOP/s"
         self.elem = 1 if c.kv.dtype == "e4m3" else 2
         self.dtype_name = "bf16" if self.elem == 2 else "fp8-e4m3 kv (widened to f16 for the products), bf16 q/out"
+        self.fp8_qk_share = 0.0
         if self.q8:
             self.dtype_name = "fp8-e4m3 q and k (kind::f8f6f4 Q K^T), v widened to f16 for P V, bf16 out"
+            self.fp8_qk_share = 0.5  # Q K^T and P V have equal flops
         self.e2e_api = "sa_prefill with pinned host q, k, v in, out/lse of both calls back"
         self.B = len(self.q_lens)
         self.maxlen = max(self.kv_lens)
@@ -906,6 +908,13 @@ def run_native(args, world, rank, local):
         # a kernel looped back to back for the whole timed region: the sustained figure
         peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
         bound, nominal = "tensor", 2250.0
+        # Q K^T on E4M3 runs at FP8 rate (2x the 16-bit rate, the nominal 4.5 / 2.25
+        # PFLOP/s ratio), P V at the 16-bit rate; half the flops each: the peak of
+        # that mix is F / (F/2 / 2P + F/2 / P) = 4/3 P
+        mix = getattr(wl, "fp8_qk_share", 0.0)
+        if mix:
+            scale = 1.0 / (mix / 2.0 + (1.0 - mix))
+            peak, nominal = peak * scale, nominal * scale
     traffic = ncu_traffic(kname, "config%d" % cfg)
 
     e2e_ms, h2d, d2h = wl.e2e(stream, max(3, min(steps, 200)), 3, flush)
@@ -932,7 +941,10 @@ def run_native(args, world, rank, local):
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "kernel": kname, ("algorithmic_bytes_per_launch" if bound == "hbm"
                                        else "algorithmic_flops_per_launch"): kbytes,
-                     "avg_launch_ms": round(k_ms, 6), "peak_source": peak_src,
+                     "avg_launch_ms": round(k_ms, 6),
+                     "peak_source": peak_src + (" bf16, scaled for FP8 Q K^T (%.0f %% of the flops at 2x rate)"
+                                                % (100 * getattr(wl, "fp8_qk_share", 0.0))
+                                                if getattr(wl, "fp8_qk_share", 0.0) else ""),
                      "frac_of_nominal": round(achieved / nominal, 4)},
         "clocks": clocks,
         "e2e": {"value": round(e2e_value, 2), "unit": wl.unit, "h2d_bytes_per_step": h2d,
