@@ -75,10 +75,22 @@ def check(r):
     assert (err <= OUT_ATOL + OUT_RTOL * np.abs(r["q_ref"])).all(), float(err.max())
     gk, gv = _cache_np(r["kvg"].k), _cache_np(r["kvg"].v)
     if r["dtype"] == "bf16":
-        # the kernel rounds fp32 to bf16, the oracle fp64 -> fp32 -> bf16: at most one ulp apart
+        # The kernel rotates in fp32 with an fp32 table and rounds to bf16; the
+        # oracle rounds its fp64 value once.  Apart from one ulp of rounding,
+        # the fp32 products of a rotation (cos and sin times the two halves)
+        # carry about 2^-24 of the row's magnitude each; where they nearly
+        # cancel, that exceeds half an ulp of the small result.  Bound:
+        # |got - want| <= ulp(want) + 2^-20 * max |row|.
         for got, want in [(gk, r["ck"]), (gv, r["cv"])]:
-            diff = np.abs(got.astype(np.int64) - want.astype(np.int64))
-            assert diff.max() <= 1, int(diff.max())
+            diff = got != want  # raw bits: NaN poison compares equal to itself here
+            if not diff.any():
+                continue
+            g64, w64 = _bf16_values(got), _bf16_values(want)
+            rowmax = np.abs(np.where(np.isfinite(w64), w64, 0.0)).max(axis=-1, keepdims=True)
+            ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(w64), 2.0 ** -126))) - 7)
+            tol = ulp + 2.0 ** -20 * np.broadcast_to(rowmax, w64.shape)
+            err = np.abs(g64 - w64)
+            assert np.all(err[diff] <= tol[diff]), float((err[diff] / tol[diff]).max())
     else:
         for got, want in [(gk, r["ck"]), (gv, r["cv"])]:
             mism = got != want
@@ -87,6 +99,11 @@ def check(r):
             a, b = got[mism].astype(np.int64), want[mism].astype(np.int64)
             assert np.all((a & 0x80) == (b & 0x80)) and np.all(np.abs((a & 0x7F) - (b & 0x7F)) == 1)
             assert mism.sum() <= max(2, got.size // 100000), int(mism.sum())
+
+
+def _bf16_values(bits):
+    """fp64 values of bf16 bit patterns (uint16 array of any shape)."""
+    return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
 def assert_untouched(r):
@@ -169,3 +186,14 @@ def test_fp8_query_output(sa):
     a, b = got[mism].astype(np.int64), want[mism].astype(np.int64)
     assert np.all((a & 0x80) == (b & 0x80)) and np.all(np.abs((a & 0x7F) - (b & 0x7F)) == 1)
     assert mism.sum() <= 4, int(mism.sum())
+
+
+def test_workload9_full_size(sa):
+    """The launch the bench times: 8192 new tokens of one sequence at positions
+    0..8191, 64 q / 8 kv heads, YaRN (theta 150000, factor 32, original 4096)
+    into a paged HND bf16 cache.  Every rotated query element and every cache
+    element is checked."""
+    r = run_case(sa, [8192], [8192], seed=506)
+    assert r["flags"] == 0
+    check(r)
+    assert_untouched(r)
