@@ -188,12 +188,13 @@ def test_fp8_query_output(sa):
     assert mism.sum() <= 4, int(mism.sum())
 
 
-def test_workload9_full_size(sa):
-    """The launch the bench times: 8192 new tokens of one sequence at positions
-    0..8191, 64 q / 8 kv heads, YaRN (theta 150000, factor 32, original 4096)
-    into a paged HND bf16 cache.  Every rotated query element and every cache
-    element is checked."""
-    r = run_case(sa, [8192], [8192], seed=506)
+@pytest.mark.parametrize("kv_dtype", ["bf16", "e4m3"])
+def test_workload9_full_size(sa, kv_dtype):
+    """The launch the bench times (bf16 cache), and the same on an E4M3 cache:
+    8192 new tokens of one sequence at positions 0..8191, 64 q / 8 kv heads,
+    YaRN (theta 150000, factor 32, original 4096) into a paged HND cache.
+    Every rotated query element and every cache element is checked."""
+    r = run_case(sa, [8192], [8192], kv_dtype=kv_dtype, seed=506)
     assert r["flags"] == 0
     check(r)
     assert_untouched(r)
