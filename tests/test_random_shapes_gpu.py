@@ -70,3 +70,29 @@ def test_random_prefill(sa, oracle, seed):
     check_close(out, lse, ref_o, ref_l, "random prefill %d: %s %s w=%d Hq/Hkv=%d/%d q=%s kv=%s paged=%s"
                 % (seed, kv_dtype, layout if paged else "contiguous", window, hq, hkv, q_lens, kv_lens, paged))
     assert sa.sa_device_status() == 0
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_random_prefill_e4m3_queries(sa, oracle, seed):
+    from test_prefill_gpu import run_q8
+    g, hq, hkv, page, layout, _, window = _draw(7000 + seed)
+    kv_lens = [int(x) for x in g.choice([1, 64, 129, 300, 700], int(g.integers(1, 4)))]
+    q_lens = [int(g.integers(1, L + 1)) for L in kv_lens]
+    case = W.make_prefill_case(q_lens, kv_lens, num_qo_heads=hq, num_kv_heads=hkv, kv_dtype="e4m3", paged=True,
+                               page_size=page, layout=layout, window=window, poison_pages=2, seed=8000 + seed)
+    run_q8(sa, oracle, case, "random E4M3-query prefill %d: %s w=%d P=%d Hq/Hkv=%d/%d q=%s kv=%s"
+           % (seed, layout, window, page, hq, hkv, q_lens, kv_lens))
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_random_rope_append(sa, seed):
+    from test_rope_gpu import assert_untouched, check, run_case
+    g = np.random.default_rng(9000 + seed)
+    hq, hkv = GROUPS[int(g.integers(len(GROUPS)))]
+    seqlens = [int(x) for x in g.choice([1, 16, 17, 300, 1029], int(g.integers(1, 5)))]
+    new = [int(g.integers(1, L + 1)) for L in seqlens]
+    r = run_case(sa, seqlens, new, kv_dtype=str(g.choice(["bf16", "e4m3"])), layout=str(g.choice(["HND", "NHD"])),
+                 hq=hq, hkv=hkv, seed=9100 + seed)
+    assert r["flags"] == 0
+    check(r)
+    assert_untouched(r)
