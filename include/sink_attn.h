@@ -33,6 +33,16 @@
  *    caller-given workspace.
  *  - Asynchrony: every call only queues kernels on `stream` and returns; none
  *    synchronises the host.  Results are ready when the stream's work is done.
+ *  - Launch chaining: every kernel of the library is launched with
+ *    programmatic stream serialization and waits for the grid before it
+ *    (griddepcontrol.wait) before touching memory, so its inputs may come from
+ *    any earlier work on the stream.  It also lets the next grid on the stream
+ *    be scheduled before it finishes (griddepcontrol.launch_dependents): a
+ *    caller's kernel launched after it WITH the programmatic-serialization
+ *    attribute must wait for its grid dependency (griddepcontrol.wait /
+ *    cudaGridDependencySynchronize) before reading this call's results.
+ *    Kernels launched without that attribute, copies and events see plain
+ *    stream order.
  *  - Errors: argument errors are detected on the host before any launch and
  *    return SA_ERR_INVALID_ARG (malformed) or SA_ERR_UNSUPPORTED (well formed
  *    but outside what the kernels handle); nothing is launched then.  A failed
