@@ -35,6 +35,16 @@ MUTANTS = {
         ("        Z = (sigma == -INFINITY) ? 0.0 : exp(sigma - M);\n        for (s = 0; s < S; ++s) {",
          "        Z = 0.0;\n        for (s = 0; s < S; ++s) {"),
     "merge weight sign": ("            w = exp(l - M);", "            w = exp(M - l);"),
+    "head and token strides swapped":
+        ("return page * kv->stride_page + (int64_t)g * kv->stride_head + slot * kv->stride_token;",
+         "return page * kv->stride_page + (int64_t)g * kv->stride_token + slot * kv->stride_head;"),
+    "split chunks overlap by one key": ("lo, lo + chunk, part_o", "lo, lo + chunk + 1, part_o"),
+    "E4M3 query scale ignored":
+        ("return sao_e4m3_to_f64(((const uint8_t *)q->row)[d]) * q->scale;",
+         "return sao_e4m3_to_f64(((const uint8_t *)q->row)[d]);"),
+    "E4M3 query bytes swapped in pairs":
+        ("return sao_e4m3_to_f64(((const uint8_t *)q->row)[d]) * q->scale;",
+         "return sao_e4m3_to_f64(((const uint8_t *)q->row)[d ^ 1]) * q->scale;"),
 }
 
 
