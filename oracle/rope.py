@@ -83,15 +83,22 @@ def rope_rotate(x, positions, inv_freq, mscale):
 
 # ---- storage encoders (own code, from the formats) ------------------------
 def bf16_bits_rne(x):
-    """fp64 -> bf16 bit patterns (uint16), round to nearest even, via fp32
-    (the value is first rounded to fp32, as a kernel holding it in fp32 does)."""
-    f = np.asarray(x, np.float64).astype(np.float32)
-    u = f.view(np.uint32).astype(np.uint64)
-    lsb = (u >> 16) & 1
-    r = (u + 0x7FFF + lsb) >> 16
-    nan = np.isnan(f)
-    r = np.where(nan, 0x7FC0, r)
-    return r.astype(np.uint16)
+    """fp64 -> bf16 bit patterns (uint16): one round-to-nearest-even of the
+    exact fp64 value to 8 significant bits (exponent range of fp32, subnormals
+    below 2^-126 in steps of 2^-133, overflow to inf past the largest finite
+    value by half an ulp), NaN -> 0x7FC0.  No intermediate rounding: a value
+    just off a bf16 midpoint goes to its nearer neighbour."""
+    x = np.asarray(x, np.float64)
+    a = np.abs(x)
+    with np.errstate(over="ignore", invalid="ignore"):
+        _, e2 = np.frexp(a)                   # a = f * 2^e2, f in [0.5, 1): a in [2^(e2-1), 2^e2)
+        qexp = np.maximum(e2 - 1, -126) - 7   # exponent of one bf16 ulp at a (fixed below 2^-126)
+        m = np.rint(np.ldexp(a, -qexp))       # exact scaling; rint rounds half to even
+        r = np.ldexp(m, qexp)                 # the rounded value, exact in fp64 (m <= 256)
+        bits = (r.astype(np.float32).view(np.uint32) >> 16).astype(np.uint32)  # exact, or inf past the range
+    bits = np.where(np.signbit(x), bits | 0x8000, bits)
+    bits = np.where(np.isnan(x), 0x7FC0, bits)
+    return bits.astype(np.uint16)
 
 
 def e4m3_encode(x):

@@ -79,6 +79,7 @@ ROPE_MUTANTS = {
     "E4M3 ties away from zero": ("    if r > 0.5 or (r == 0.5 and f % 2 == 1):", "    if r >= 0.5:"),
     "E4M3 saturates to the NaN code": ("o[n] = sign | 0x7E", "o[n] = sign | 0x7F"),
     "cache slot ignores the page size": ("(p % P) * cache[\"stride_token\"]", "(p % 16) * cache[\"stride_token\"]"),
+    "bf16 rounded through fp32 first": ("    a = np.abs(x)\n    with np.errstate", "    a = np.abs(x.astype(np.float32).astype(np.float64))\n    with np.errstate"),
 }
 
 

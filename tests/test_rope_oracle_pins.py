@@ -3,7 +3,8 @@ facts that do not come from its own code: the closed form of plain rotary
 embeddings, the relative-position identity that defines them, norm
 preservation, the YaRN paper's description of which dimensions keep and which
 interpolate their frequency, the E4M3 format (all codes, and torch's float8
-cast), and a brute-force cache write."""
+cast), and a brute-force cache write; bf16 storage as one rounding of the exact value
+(brute force by exact rational distances)."""
 import importlib.util
 import math
 import os
@@ -104,10 +105,55 @@ def test_e4m3_encoder_round_trips_every_code_and_matches_torch():
 
 
 def test_bf16_rounding_matches_torch():
-    x = np.random.default_rng(4).standard_normal(10000) * 10
+    # fp32-exact inputs: torch rounds fp64 through fp32, which is then exact
+    x = (np.random.default_rng(4).standard_normal(10000) * 10).astype(np.float32).astype(np.float64)
     ours = R.bf16_bits_rne(x)
     theirs = torch.tensor(x.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     assert np.array_equal(ours, theirs)
+
+
+def _bf16_nearest_brute_force(xs):
+    """Bit patterns of the bf16 values nearest to each x, by exact rational
+    distances to the two neighbouring bf16 values; ties go to the even
+    pattern.  The bf16 values are torch's decoding of every pattern (an exact
+    widening); inf stands at 2^128, the next value past the largest finite
+    one.  Sign by symmetry."""
+    from fractions import Fraction
+    pats = np.arange(0, 0x7F81, dtype=np.uint16)
+    vals = torch.tensor(pats.view(np.int16)).view(torch.bfloat16).double().numpy()
+    vals[-1] = 2.0 ** 128
+    out = []
+    for x in xs:
+        a = abs(float(x))
+        j = int(np.searchsorted(vals, a))
+        if j < len(vals) and vals[j] == a:
+            best = j
+        else:
+            lo, hi = j - 1, j
+            dl, dh = Fraction(a) - Fraction(vals[lo]), Fraction(vals[hi]) - Fraction(a)
+            best = lo if dl < dh else hi if dh < dl else (lo if lo % 2 == 0 else hi)
+        out.append(best | (0x8000 if math.copysign(1.0, x) < 0 else 0))
+    return np.array(out, np.uint16)
+
+
+def test_bf16_rounding_is_one_rounding_of_the_exact_value():
+    """The cache stores the fp64 value rounded once.  Inputs a hair off a bf16
+    midpoint (relative 2^-40, inside half an fp32 ulp) are the ones where a
+    rounding through fp32 first lands on the midpoint and then goes to even:
+    the nearer neighbour is required, the brute force decides it."""
+    g = np.random.default_rng(6)
+    pats = np.concatenate([g.integers(1, 0x7F7F, 1500), np.arange(1, 8), np.arange(0x7F70, 0x7F7F)]).astype(np.uint16)
+    lo = torch.tensor(pats.view(np.int16)).view(torch.bfloat16).double().numpy()
+    hi = torch.tensor((pats + 1).astype(np.uint16).view(np.int16)).view(torch.bfloat16).double().numpy()
+    mid = (lo + hi) / 2  # exact in fp64
+    xs = np.concatenate([mid * (1 + 2.0 ** -40), mid * (1 - 2.0 ** -40), mid, lo + (hi - lo) * g.random(len(lo))])
+    xs = np.concatenate([xs, -xs[::7], [2.0 ** 128 * (1 - 2.0 ** -9), 2.0 ** 128 * (1 - 2.0 ** -9) * (1 - 2.0 ** -40)]])
+    want = _bf16_nearest_brute_force(xs)
+    assert np.array_equal(R.bf16_bits_rne(xs), want)
+    # these inputs do separate one rounding from two: through fp32 first, the
+    # off-midpoint ones with an odd lower neighbour come out differently
+    via32 = torch.tensor(xs.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert (via32 != want).sum() > 500
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "e4m3"])
