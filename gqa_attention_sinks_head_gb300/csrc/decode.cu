@@ -591,18 +591,12 @@ template <bool FP8, int kStages, int TPW, bool kJoint>
 cudaError_t prepare_decode()
 {
     // one cudaFuncSetAttribute per device and variant
-    static int done[64] = {0};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess)
-        return e;
-    if (dev >= 0 && dev < 64 && done[dev])
-        return cudaSuccess;
-    e = cudaFuncSetAttribute(decode_kernel<FP8, kStages, TPW, kJoint>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(decode_smem_bytes<FP8, kStages>()));
-    if (e == cudaSuccess && dev >= 0 && dev < 64)
-        done[dev] = 1;
-    return e;
+    static std::atomic<int> done[kMaxDevices];
+    return once_per_device(done, [] {
+        return cudaFuncSetAttribute(decode_kernel<FP8, kStages, TPW, kJoint>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(decode_smem_bytes<FP8, kStages>()));
+    });
 }
 
 template <bool FP8, int kStages>

@@ -634,19 +634,13 @@ template <bool FP8, bool Q8>
 cudaError_t launch_of(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, const PrefillParams &p,
                       cudaStream_t stream)
 {
-    static int done[64] = {0};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    static std::atomic<int> done[kMaxDevices];  // one cudaFuncSetAttribute per device and variant
+    const cudaError_t e = once_per_device(done, [] {
+        return cudaFuncSetAttribute(prefill_kernel<FP8, Q8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(prefill_smem_bytes<FP8>()));
+    });
     if (e != cudaSuccess)
         return e;
-    if (dev < 0 || dev >= 64 || !done[dev]) {
-        e = cudaFuncSetAttribute(prefill_kernel<FP8, Q8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(prefill_smem_bytes<FP8>()));
-        if (e != cudaSuccess)
-            return e;
-        if (dev >= 0 && dev < 64)
-            done[dev] = 1;
-    }
     const dim3 grid(p.num_qo_heads / p.heads_per_cta, p.num_q_tiles, p.batch);
     return launch_pdl(prefill_kernel<FP8, Q8>, grid, dim3(kThreads), prefill_smem_bytes<FP8>(), stream, tq, tk, tv, p);
 }

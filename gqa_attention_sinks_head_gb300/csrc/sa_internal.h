@@ -6,6 +6,7 @@
 #include <cuda_runtime_api.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <utility>
 
 #include "../../include/sink_attn.h"
@@ -58,6 +59,7 @@ struct PrefillParams {
     int32_t batch, num_qo_heads, num_kv_heads, group, heads_per_cta;
     int32_t page_size, table_stride, num_pages, max_q_len, max_kv_len;
     int32_t window, num_q_tiles;
+    int32_t box_rows;                       // keys per K / V tensor-map box: 16, or 64 when a 64-key tile lies in one page
     int32_t dim_token, dim_head, dim_page;  // tensor-map dimension (1..3) of each KV coordinate
     float score_scale;                      // sm_scale * log2(e) (* k_scale for an FP8 cache)
     float out_scale;                        // 1 (v_scale for an FP8 cache)
@@ -103,6 +105,28 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// Runs `set` (a per-kernel cudaFuncSetAttribute) once per device: `flags`
+// is a static array owned by the caller, indexed by device.  The flag is
+// atomic, so concurrent first calls from several host threads are well
+// defined: each may run `set`, which the runtime allows from any thread and
+// which is idempotent, and every later call sees the flag and skips it.
+constexpr int kMaxDevices = 64;
+template <typename F>
+cudaError_t once_per_device(std::atomic<int> (&flags)[kMaxDevices], F &&set)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    const bool tracked = dev >= 0 && dev < kMaxDevices;
+    if (tracked && flags[dev].load(std::memory_order_acquire) != 0)
+        return cudaSuccess;
+    e = set();
+    if (e == cudaSuccess && tracked)
+        flags[dev].store(1, std::memory_order_release);
+    return e;
 }
 
 // Launchers (return the launch error, if any).

@@ -11,7 +11,7 @@ import pytest
 import torch
 
 import workloads as W
-from sa_testlib import check_close
+from sa_testlib import check_close, oracle_decode
 
 pytestmark = pytest.mark.gpu
 
@@ -33,16 +33,20 @@ def _both(sa, case, splits):
     return out, lse, ref_out, ref_lse, need
 
 
-def test_static_workspace_matches_sa_decode_twice_in_a_row(sa):
-    # two different calls back to back: the second must not see the first's leftovers
-    a = W.make_decode_case([1, 300, 1500, 4000], page_size=16, window=0, poison_pages=3, seed=300).to("cuda")
-    b = W.make_decode_case([2000, 17, 900], page_size=16, window=128, kv_dtype="e4m3", seed=301).to("cuda")
-    c = W.make_decode_case([5000, 64, 3333, 1, 777, 2048], page_size=16, window=0, seed=302).to("cuda")
-    for case, splits in [(a, 7), (b, 3), (c, 0), (a, 7)]:
-        out, lse, ref_out, ref_lse, need = _both(sa, case, splits)
-        assert need <= sa.SA_STATIC_WORKSPACE_BYTES
-        check_close(out, lse, ref_out.double().cpu().numpy(), ref_lse.double().cpu().numpy(),
-                    "static workspace, splits=%d" % splits)
+def test_static_workspace_matches_sa_decode_twice_in_a_row(sa, oracle):
+    # different calls back to back: a later call must not see an earlier one's leftovers
+    cases = [W.make_decode_case([1, 300, 1500, 4000], page_size=16, window=0, poison_pages=3, seed=300),
+             W.make_decode_case([2000, 17, 900], page_size=16, window=128, kv_dtype="e4m3", seed=301),
+             W.make_decode_case([5000, 64, 3333, 1, 777, 2048], page_size=16, window=0, seed=302)]
+    refs = [oracle_decode(oracle, c) for c in cases]
+    gpu = [c.to("cuda") for c in cases]
+    for i, splits in [(0, 7), (1, 3), (2, 0), (0, 7), (2, 5)]:
+        out, lse, ref_out, ref_lse, need = _both(sa, gpu[i], splits)
+        assert 0 < need <= sa.SA_STATIC_WORKSPACE_BYTES or splits == 0
+        # the same kernels with the same split: bit for bit what sa_decode gives
+        assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16)), "out differs from sa_decode"
+        assert torch.equal(lse.view(torch.int32), ref_lse.view(torch.int32)), "lse differs from sa_decode"
+        check_close(out, lse, refs[i][0], refs[i][1], "static workspace vs oracle, case %d splits=%d" % (i, splits))
     assert sa.sa_device_status() == 0
 
 
