@@ -115,14 +115,21 @@ class ClockSampler:
 
     def stop(self):
         if self.proc is None:
-            return None
+            return
         time.sleep(0.25)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        inside = [s for t, s in self.samples if self.t0 is not None and self.t0 - 0.15 <= t <= self.t1 + 0.15]
+        self.proc = None
+
+    def summary(self, t0=None, t1=None):
+        """Median SM clock, max clock and throttle reasons of the samples taken
+        inside [t0, t1] (the timed region), or of all samples if none fell in it."""
+        t0 = self.t0 if t0 is None else t0
+        t1 = self.t1 if t1 is None else t1
+        inside = [s for t, s in self.samples if t0 is not None and t0 - 0.15 <= t <= t1 + 0.15]
         rows = inside or [s for _, s in self.samples]
         if not rows:
             return None
@@ -175,9 +182,9 @@ L2_FLUSH_BYTES = 256 << 20  # about twice the GB300's 129 MB L2
 
 
 def timed_loop(torch, stream, one, steps, warmup, flush=None):
-    """Mean device time (ms) of one() over `steps` iterations after `warmup`,
-    each bracketed by CUDA events on `stream`; flush() (if any) runs before
-    each iteration, outside its events."""
+    """Median device time (ms) of one() over `steps` iterations after
+    `warmup`, each bracketed by CUDA events on `stream`; flush() (if any) runs
+    before each iteration, outside its events."""
     with torch.cuda.stream(stream):
         for _ in range(warmup):
             one()
@@ -190,7 +197,7 @@ def timed_loop(torch, stream, one, steps, warmup, flush=None):
             one()
             e1.record(stream)
         torch.cuda.synchronize()
-    return sum(e0.elapsed_time(e1) for e0, e1 in evs) / steps
+    return statistics.median(e0.elapsed_time(e1) for e0, e1 in evs)
 
 
 class Packed:
@@ -282,7 +289,9 @@ def workload_name(cfg):
 
 
 class DecodeBench:
-    """One step = the decode calls of the workload on one resident cache."""
+    """One step = the decode calls of the workload on one resident cache.
+    With sa=None (the reference arm) only the inputs are built: the same
+    seeded bytes, drawn on the same device, and no library call is made."""
 
     def __init__(self, sa, cfg, device):
         import torch
@@ -290,6 +299,7 @@ class DecodeBench:
         self.sa, self.cfg, self.torch = sa, cfg, torch
         gen_dev = device if cfg in (2, 4, 5) else "cpu"
         self.case = W.make_config(cfg, window=0, device=gen_dev).to(device)
+        self.sample_units = len(self.case.seqlens)
         c = self.case
         self.B, self.Hq, self.D = c.q.shape
         self.Hkv = c.kv.num_kv_heads
@@ -298,6 +308,10 @@ class DecodeBench:
         self.elem = 1 if c.kv.dtype == "e4m3" else 2
         self.calls = []
         for w in windows_of(cfg):
+            if sa is None:
+                self.calls.append(dict(window=w, S=1, bytes=decode_bytes(self.seqlens, w, self.Hkv, self.Hq, self.D,
+                                                                         self.elem)))
+                continue
             S = sa.sa_decode_num_splits(self.B, self.Hkv, self.maxlen, w)
             out = torch.empty(self.B, self.Hq, self.D, dtype=torch.bfloat16, device=device)
             lse = torch.empty(self.B, self.Hq, dtype=torch.float32, device=device)
@@ -449,6 +463,7 @@ class MultiDecodeBench:
         self.Hkv = c.kv.num_kv_heads
         self.seqlens = [int(x) for x in c.seqlens.cpu()]
         self.B = len(self.seqlens)
+        self.sample_units = self.B
         self.q_len = self.R // self.B
         self.maxlen = max(self.seqlens)
         self.elem = 1 if c.kv.dtype == "e4m3" else 2
@@ -581,6 +596,7 @@ class RopeBench:
         self.unit = "GB/s"
         self.elem = 2
         self.B = 1
+        self.sample_units = T // 32
         self.maxlen = T
         self.dtype_name = "bf16 (fp32 rotation)"
         self.e2e_api = "sa_rope_append with pinned host q/k/v/positions in, rotated q back; cache resident"
@@ -664,14 +680,16 @@ def make_bench(sa, cfg, device):
 
 
 class PrefillBench:
-    """One step = the prefill calls of the workload (full context, then window 128)."""
+    """One step = the prefill calls of the workload (full context, then window
+    128), or the calls of the given windows only.  With sa=None (the reference
+    arm) only the inputs are built."""
 
-    def __init__(self, sa, cfg, device):
+    def __init__(self, sa, cfg, device, windows=None, case=None):
         import torch
         import workloads as W
         self.sa, self.cfg, self.torch = sa, cfg, torch
         self.q8 = cfg == 10
-        self.case = W.make_config(7 if self.q8 else cfg, window=0, device=device)
+        self.case = case if case is not None else W.make_config(7 if self.q8 else cfg, window=0, device=device)
         c = self.case
         self.T, self.Hq, self.D = c.q.shape
         if self.q8:  # per-tensor E4M3 codes of q (scale = amax / 448, nearest-even cast)
@@ -681,10 +699,13 @@ class PrefillBench:
         cu = c.cu_seqlens_q.cpu()
         self.q_lens = [int(x) for x in (cu[1:] - cu[:-1])]
         self.kv_lens = [int(x) for x in c.seqlens.cpu()]
+        self.sample_units = self.T
         self.calls = []
-        for w in windows_of(cfg):
-            out = torch.empty(self.T, self.Hq, self.D, dtype=torch.bfloat16, device=device)
-            lse = torch.empty(self.T, self.Hq, dtype=torch.float32, device=device)
+        for w in (windows_of(cfg) if windows is None else windows):
+            out = lse = None
+            if sa is not None:
+                out = torch.empty(self.T, self.Hq, self.D, dtype=torch.bfloat16, device=device)
+                lse = torch.empty(self.T, self.Hq, dtype=torch.float32, device=device)
             self.calls.append(dict(window=w, out=out, lse=lse,
                                    flops=prefill_flops(self.q_lens, self.kv_lens, w, self.Hq, self.D)))
         self.step_flops = sum(cl["flops"] for cl in self.calls)
@@ -696,7 +717,12 @@ class PrefillBench:
         if self.q8:
             self.dtype_name = "fp8-e4m3 q and k (kind::f8f6f4 Q K^T), v widened to f16 for P V, bf16 out"
             self.fp8_qk_share = 0.5  # Q K^T and P V have equal flops
-        self.e2e_api = "sa_prefill with pinned host q, k, v in, out/lse of both calls back"
+        self.e2e_api = "sa_prefill with pinned host q, k, v in, out/lse of every call back"
+        self.label = None
+        if windows is not None:  # a sub-step of the workload: name its calls
+            base = workload_name(cfg).split(", step =")[0]
+            self.label = "%s, call%s %s" % (base, "s" if len(windows) > 1 else "",
+                                            " + ".join("w=%d" % w for w in windows))
         self.B = len(self.q_lens)
         self.maxlen = max(self.kv_lens)
         # algorithmic bytes of a call: q in, out and lse back, and the K/V rows
@@ -741,6 +767,13 @@ class PrefillBench:
 
     def dominant(self):
         return 0, "prefill_kernel", self.calls[0]["flops"]
+
+    def bound_of(self, i):
+        """The roofline that bounds call i: a full-context call is a dense
+        contraction (tensor), a window-128 call does about 111 flop per HBM
+        byte, below the ridge (hbm)."""
+        cl = self.calls[i]
+        return "tensor" if cl["flops"] / cl["bytes"] > 300 else "hbm"
 
     def segment_names(self):
         return ["prefill w=%d" % cl["window"] for cl in self.calls]
@@ -787,10 +820,11 @@ class PrefillBench:
         import numpy as np
         import oracle
         oracle.build()
-        c = self.case
-        cpu = c.to("cpu")
+        if getattr(self, "_cpu_case", None) is None:
+            self._cpu_case = self.case.to("cpu")
+        cpu = self._cpu_case
         rows = oracle.prefill_rows(cpu.cu_seqlens_q, cpu.seqlens)
-        n = 64 if max_seqs is None else max(1, max_seqs)
+        n = 64 if max_seqs is None else max(1, min(self.T, max_seqs))
         sel = np.linspace(0, self.T - 1, n).astype(np.int32)
         t0 = time.time()
         flops = 0
@@ -808,22 +842,54 @@ class PrefillBench:
                 nk = p + 1 if cl["window"] <= 0 else min(cl["window"], p + 1)
                 flops += 4 * self.Hq * self.D * nk
         dt = time.time() - t0
-        return dt, flops, "%d of %d query rows x %d heads, both calls" % (len(sel), self.T, self.Hq)
+        return dt, flops, "%d of %d query rows x %d heads, every call (windows %s)" % (
+            len(sel), self.T, self.Hq, [cl["window"] for cl in self.calls])
 
 
 # ------------------------------------------------------------------- main
-def run_native(args, world, rank, local):
+def cpu_baseline(wl, budget_s):
+    """The oracle, as it stands, on a bounded sample of the workload: the
+    sample grows (doubling from one unit: a sequence, a query row, 32 tokens)
+    until one sample takes a tenth of the budget, then repeats until the
+    budget is spent.  Returns (amount in the workload's unit, seconds,
+    description)."""
+    import oracle
+    n, dt, amount, reps, desc = 1, 0.0, 0.0, 0, ""
+    while True:
+        d1, a1, desc = wl.oracle_sample(budget_s, max_seqs=n)
+        dt, amount, reps = dt + d1, amount + a1, reps + 1
+        if d1 >= budget_s / 10 or n >= wl.sample_units or dt >= budget_s:
+            break
+        n = min(2 * n, wl.sample_units)
+    while dt < budget_s and reps < 1000:
+        d1, a1, desc = wl.oracle_sample(budget_s, max_seqs=n)
+        dt, amount, reps = dt + d1, amount + a1, reps + 1
+    scale = 1e9 if wl.unit == "GB/s" else 1e12
+    return {"value": round(amount / scale / dt, 6), "unit": wl.unit,
+            "cores": getattr(wl, "oracle_cores", 0) or oracle.num_threads(), "kind": "oracle",
+            "sample": "%s; timed %d times" % (desc, reps), "seconds": round(dt, 2)}
+
+
+def workload_config(cfg, wl, world):
+    """The workload the line is quoted on (identical in both arms)."""
+    return {"workload": getattr(wl, "label", None) or workload_name(cfg), "global_batch": wl.B * world,
+            "seq_len_max": wl.maxlen,
+            "parallelism": "replicas" if world > 1 else "single GPU"}
+
+
+def measure(wl, cfg, args, world, rank, stream, sampler, steps, cpu_budget_s):
+    """Times one workload on this GPU and returns its record.
+
+    Two passes of K steps after W warm-up steps.  The first times whole steps
+    with CUDA events on the launching stream at step boundaries only (no event
+    between a step's launches): the step time is the median over the K steps
+    (the mean is given beside it), and `value` = the step's algorithmic work /
+    that time.  The second repeats the steps with an event after every launch
+    segment: the dominant kernel's average launch time and the per-segment
+    breakdown.  Inputs under twice the L2 size are evicted before every step,
+    outside the events."""
     import torch
-    import gqa_attention_sinks_head_gb300 as sa
-    sa.build()
-    sa.load()
-    torch.cuda.set_device(local)
-    dist_init(world, "nccl")
-    cfg = args.config
-    wl = make_bench(sa, cfg, "cuda")
-    stream = torch.cuda.Stream()
-    steps = args.steps
-    sampler = ClockSampler(local) if rank == 0 else None
+    peaks, peak_src = load_peaks()
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
             wl.step(stream)
@@ -840,13 +906,7 @@ def run_native(args, world, rank, local):
         def flush():
             flush_buf.zero_()
             flush_rd.sum()
-    ci, kname, kbytes = wl.dominant()
-    # The step is a short list of launch segments (a kernel, or a call); events
-    # between the segments time the step and its dominant kernel on the
-    # launching stream.  --graph captures each segment once as a CUDA graph
-    # and replays it (measured: no faster here, since the L2 flush before each
-    # step leaves the host ahead of the device, and it drops the programmatic
-    # launch overlap of the decode merge).
+    ci, kname, kwork = wl.dominant()
     segs = wl.segments(stream)
     runs = list(segs)
     if args.graph:
@@ -857,17 +917,11 @@ def run_native(args, world, rank, local):
                 fn()
             runs.append(g.replay)
         torch.cuda.synchronize()
-    # Two passes of K steps each.  The first times whole steps, with events
-    # only at step boundaries (so that no event sits between the launches of
-    # a step): the step time and `value`.  The second repeats the steps with
-    # an event after every segment: the dominant kernel's time and the
-    # segment breakdown.
     step_evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(runs) + 1)] for _ in range(steps)]
     dist_barrier(world)
     torch.cuda.synchronize()
-    if sampler:
-        sampler.begin()
+    t_begin = time.time()
     with torch.cuda.stream(stream):  # the timed region: K steps
         for i in range(steps):
             if flush is not None:
@@ -877,6 +931,7 @@ def run_native(args, world, rank, local):
                 run()
             step_evs[i][1].record(stream)
     torch.cuda.synchronize()
+    t_end = time.time()
     dist_barrier(world)
     with torch.cuda.stream(stream):  # the segment breakdown: K more steps
         for i in range(steps):
@@ -887,27 +942,27 @@ def run_native(args, world, rank, local):
                 run()
                 evs[i][j + 1].record(stream)
     torch.cuda.synchronize()
-    if sampler:
-        sampler.end()
     dist_barrier(world)
-    ms = statistics.fmean(e[0].elapsed_time(e[1]) for e in step_evs)
-    ms_median = statistics.median(e[0].elapsed_time(e[1]) for e in step_evs)
+    step_ms = [e[0].elapsed_time(e[1]) for e in step_evs]
+    ms = dist_max(statistics.median(step_ms), world)
+    ms_mean = dist_max(statistics.fmean(step_ms), world)
     seg_ms = [statistics.fmean(e[j].elapsed_time(e[j + 1]) for e in evs) for j in range(len(runs))]
-    ms = dist_max(ms, world)
     k_ms = statistics.fmean(e[ci].elapsed_time(e[ci + 1]) for e in evs)
-    clocks = sampler.stop() if sampler else None
 
-    peaks, peak_src = load_peaks()
-    value = wl.amount() * world / (ms / 1e3)
-    if wl.unit == "GB/s":
+    bound = wl.bound_of(0) if hasattr(wl, "bound_of") else ("hbm" if wl.unit == "GB/s" else "tensor")
+    if bound == "hbm":
+        kbytes = kwork if wl.unit == "GB/s" else wl.calls[0]["bytes"]
         achieved = kbytes / 1e9 / (k_ms / 1e3)
         peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
-        bound, nominal = "hbm", 8000.0
+        nominal, runit, peak_name = 8000.0, "GB/s", "hbm_gbs"
+        work_key, work = "algorithmic_bytes_per_launch", kbytes
     else:
-        achieved = kbytes / 1e12 / (k_ms / 1e3)
-        # a kernel looped back to back for the whole timed region: the sustained figure
-        peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
-        bound, nominal = "tensor", 2250.0
+        achieved = kwork / 1e12 / (k_ms / 1e3)
+        # one isolated launch of under a millisecond behind an L2 flush, not a
+        # seconds-long loop: the burst figure
+        peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+        nominal, runit, peak_name = 2250.0, "TFLOP/s", "bf16_tflops (burst)"
+        work_key, work = "algorithmic_flops_per_launch", kwork
         # Q K^T on E4M3 runs at FP8 rate (2x the 16-bit rate, the nominal 4.5 / 2.25
         # PFLOP/s ratio), P V at the 16-bit rate; half the flops each: the peak of
         # that mix is F / (F/2 / 2P + F/2 / P) = 4/3 P
@@ -915,42 +970,33 @@ def run_native(args, world, rank, local):
         if mix:
             scale = 1.0 / (mix / 2.0 + (1.0 - mix))
             peak, nominal = peak * scale, nominal * scale
+            peak_name += ", scaled for FP8 Q K^T (%.0f %% of the flops at 2x rate)" % (100 * mix)
     traffic = ncu_traffic(kname, "config%d" % cfg)
 
     e2e_ms, h2d, d2h = wl.e2e(stream, max(3, min(steps, 200)), 3, flush)
-    e2e_value = wl.amount() * world / (e2e_ms / 1e3)
-
-    line = {
-        "metric": METRIC, "value": round(value, 2), "unit": wl.unit, "n_gpus": world, "steps": steps,
-        "warmup": args.warmup, "ms_per_step": round(ms, 6), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": wl.dtype_name,
-        "data": "synthetic (seeded; N(0,1) q/k/v, sinks U(-2,6)); no weights or datasets",
-        "config": {"workload": workload_name(cfg), "global_batch": wl.B * world, "seq_len_max": wl.maxlen,
-                   "parallelism": "replicas" if world > 1 else "single GPU",
-                   "splits": [cl.get("S", 1) for cl in wl.calls],
+    rec = {
+        "value": round(wl.amount() * world / (ms / 1e3), 2), "unit": wl.unit, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 6), "ms_per_step_mean": round(ms_mean, 6),
+        "dtype": wl.dtype_name, "config": workload_config(cfg, wl, world),
+        "method": {"splits": [cl.get("S", 1) for cl in wl.calls],
                    "l2": ("flushed before every step (256 MB write, then a 256 MB read of another buffer so "
                           "that no dirty line is left to write back; outside the step's events)"
                           if flush_buf is not None else
                           "inputs larger than twice the L2 (%.2f GB per step); no flush" % (wl.resident_bytes() / 1e9)),
                    "launch": "each launch segment of the step captured as a CUDA graph and replayed"
                              if args.graph else "eager",
-                   "timing": "CUDA events around each step on its stream, none between a step's launches; mean "
-                             "over the K steps. A second pass of K steps with an event after every launch segment "
-                             "times the dominant kernel and the segments."},
-        "roofline": {"bound": bound, "achieved": round(achieved, 1), "peak": peak, "unit": wl.unit,
-                     "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": kname, ("algorithmic_bytes_per_launch" if bound == "hbm"
-                                       else "algorithmic_flops_per_launch"): kbytes,
-                     "avg_launch_ms": round(k_ms, 6),
-                     "peak_source": peak_src + (" bf16, scaled for FP8 Q K^T (%.0f %% of the flops at 2x rate)"
-                                                % (100 * getattr(wl, "fp8_qk_share", 0.0))
-                                                if getattr(wl, "fp8_qk_share", 0.0) else ""),
+                   "timing": "CUDA events around each step on its stream, none between a step's launches; "
+                             "ms_per_step and value from the median of the K steps (mean beside it). A second "
+                             "pass of K steps with an event after every launch segment times the dominant kernel "
+                             "(avg_launch_ms, a mean) and the segments."},
+        "roofline": {"bound": bound, "achieved": round(achieved, 1), "peak": peak, "unit": runit,
+                     "frac": round(achieved / peak, 4), "traffic": traffic, "kernel": kname, work_key: work,
+                     "avg_launch_ms": round(k_ms, 6), "peak_source": "%s %s" % (peak_src, peak_name),
                      "frac_of_nominal": round(achieved / nominal, 4)},
-        "clocks": clocks,
-        "e2e": {"value": round(e2e_value, 2), "unit": wl.unit, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "api": wl.e2e_api},
-        "gpu_launches": steps * wl.kernels_per_step,  # timed region; the library's kernels (the L2 flush is torch's)
-        "ms_per_step_median": round(ms_median, 6),
+        "clocks": sampler.summary(t_begin, t_end) if sampler else None,
+        "e2e": {"value": round(wl.amount() * world / (e2e_ms / 1e3), 2), "unit": wl.unit,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "api": wl.e2e_api},
+        "gpu_launches": steps * wl.kernels_per_step,  # the library's kernels in the timed region (the flush is torch's)
         "segments": [{"name": n, "ms": round(t, 6)} for n, t in
                      zip(getattr(wl, "segment_names", lambda: ["segment %d" % j for j in range(len(seg_ms))])(),
                          seg_ms)],
@@ -958,31 +1004,72 @@ def run_native(args, world, rank, local):
     if hasattr(wl, "notes"):
         notes = wl.notes(seg_ms, peaks)
         if notes:
-            line["notes"] = notes
+            rec["notes"] = notes
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        import oracle
-        # repeat the sample until about 10 s of host work is timed
-        dt, nbytes, reps = 0.0, 0, 0
-        while dt < 10.0 and reps < 1000:
-            d1, b1, desc = wl.oracle_sample(30.0)
-            dt, nbytes, reps = dt + d1, nbytes + b1, reps + 1
-        line["cpu_baseline"] = {"value": round(nbytes / (1e9 if wl.unit == "GB/s" else 1e12) / dt, 6),
-                                "unit": wl.unit,
-                                "cores": getattr(wl, "oracle_cores", 0) or oracle.num_threads(), "kind": "oracle",
-                                "sample": "%s; timed %d times" % (desc, reps),
-                                "seconds": round(dt, 2)}
+        rec["cpu_baseline"] = cpu_baseline(wl, cpu_budget_s)
         if cfg == 1:  # the smallest workload: the oracle on one thread as well
+            import oracle
             cores = oracle.num_threads()
             oracle.set_num_threads(1)
             try:
-                dt1, nb1, reps1 = 0.0, 0, 0
-                while dt1 < 3.0 and reps1 < 1000:
-                    d1, b1, _ = wl.oracle_sample(30.0)
-                    dt1, nb1, reps1 = dt1 + d1, nb1 + b1, reps1 + 1
+                rec["cpu_baseline"]["single_thread_value"] = cpu_baseline(wl, 3.0)["value"]
             finally:
                 oracle.set_num_threads(cores)
-            line["cpu_baseline"]["single_thread_value"] = round(nb1 / 1e9 / dt1, 6)
+    return rec
+
+
+HEADLINE = 4  # decode B=128, L=32768: the largest single-GPU decode workload
+
+
+def run_native(args, world, rank, local):
+    import torch
+    import gqa_attention_sinks_head_gb300 as sa
+    sa.build()
+    sa.load()
+    torch.cuda.set_device(local)
+    dist_init(world, "nccl")
+    stream = torch.cuda.Stream()
+    sampler = ClockSampler(local) if rank == 0 else None
+    if args.config is not None:  # one workload
+        cfg = args.config
+        steps = args.steps if args.steps is not None else DEFAULT_STEPS[cfg]
+        rec = measure(make_bench(sa, cfg, "cuda"), cfg, args, world, rank, stream, sampler, steps, 10.0)
+        subs = {}
+    else:
+        # The default line: decode B=128, L=32768 (split-KV) as the headline;
+        # then, as sub-records with their own roofline, cpu_baseline and e2e,
+        # the B=64 ragged decode step (full context and window 128) and each
+        # call of the T=8192 prefill.
+        def steps_of(cfg):
+            return args.steps if args.steps is not None else DEFAULT_STEPS[cfg]
+        wl = make_bench(sa, HEADLINE, "cuda")
+        rec = measure(wl, HEADLINE, args, world, rank, stream, sampler, steps_of(HEADLINE), 10.0)
+        del wl
+        torch.cuda.empty_cache()
+        subs = {}
+        wl = make_bench(sa, 2, "cuda")
+        subs["decode_ragged"] = measure(wl, 2, args, world, rank, stream, sampler, steps_of(2), 6.0)
+        del wl
+        torch.cuda.empty_cache()
+        import workloads as W
+        case = W.make_config(3, window=0, device="cuda")
+        calls = []
+        for w in (0, 128):
+            wl = PrefillBench(sa, 3, "cuda", windows=[w], case=case)
+            r = measure(wl, 3, args, world, rank, stream, sampler, steps_of(3), 6.0)
+            r["window"] = w
+            calls.append(r)
+            del wl
+        subs["prefill"] = {"workload": workload_name(3), "calls": calls}
+    if sampler:
+        sampler.stop()
     if rank == 0:
+        line = {"metric": METRIC, "value": rec["value"], "unit": rec["unit"], "n_gpus": world,
+                "steps": rec["steps"], "warmup": rec["warmup"], "ms_per_step": rec["ms_per_step"],
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": rec["dtype"],
+                "data": "synthetic (seeded; N(0,1) q/k/v, sinks U(-2,6)); no weights or datasets"}
+        line.update({k: v for k, v in rec.items() if k not in line})
+        line.update(subs)
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
@@ -991,50 +1078,43 @@ def run_native(args, world, rank, local):
 
 def run_reference(args, world, rank, local):
     """The oracle, as it stands, timed on the host cores on the native arm's
-    workload; each step is a bounded sample of it."""
+    headline workload (the same seeded bytes, drawn with torch on the same
+    device); each step is a bounded sample of it.  The CUDA library is not
+    loaded."""
     if rank != 0:
         return
     import torch
-    import gqa_attention_sinks_head_gb300 as sa
     import oracle
-    cfg = args.config
+    cfg = HEADLINE if args.config is None else args.config
     oracle.build()
-    sa.build()
-    sa.load()
     dev = "cuda" if torch.cuda.is_available() else "cpu"
-
-    class _Shim:  # the CPU arm only needs the split count for the byte formula
-        def __init__(self):
-            self.inner = sa
-
-        def __getattr__(self, k):
-            return getattr(self.inner, k)
-
-    wl = make_bench(_Shim(), cfg, dev)
+    wl = make_bench(None, cfg, dev)
     total_budget = float(args.budget_s)
-    steps, warmup = args.steps, args.warmup
-    # size the per-step sample from a one-sequence pilot
-    dt1, b1, _ = wl.oracle_sample(5.0, max_seqs=1)
+    steps = args.steps if args.steps is not None else DEFAULT_STEPS[cfg]
+    warmup = args.warmup
+    # size the per-step sample from a one-unit pilot
+    dt1, _, _ = wl.oracle_sample(5.0, max_seqs=1)
     per_step = total_budget / max(1, steps + warmup)
-    n = max(1, min(wl.B if cfg not in PREFILL_CONFIGS + ROPE_CONFIGS else 4096, int(per_step / max(dt1, 1e-6))))
+    n = max(1, min(wl.sample_units, int(per_step / max(dt1, 1e-6))))
     for _ in range(warmup):
         wl.oracle_sample(per_step, max_seqs=n)
     t0 = time.time()
-    nbytes = 0
+    amount = 0
     desc = ""
     for _ in range(steps):
-        _, nb, desc = wl.oracle_sample(per_step, max_seqs=n)
-        nbytes += nb
+        _, a, desc = wl.oracle_sample(per_step, max_seqs=n)
+        amount += a
     dt = time.time() - t0
-    value = nbytes / (1e9 if wl.unit == "GB/s" else 1e12) / dt
+    value = amount / (1e9 if wl.unit == "GB/s" else 1e12) / dt
     line = {
         "metric": METRIC, "value": round(value, 4), "unit": wl.unit, "n_gpus": world, "steps": steps,
         "warmup": warmup, "ms_per_step": round(dt / steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded), same bytes as the native arm",
-        "config": {"workload": workload_name(cfg), "global_batch": wl.B, "seq_len_max": wl.maxlen},
+        "config": workload_config(cfg, wl, 1),
         "impl": "reference",
-        "cpu_baseline": {"value": round(value, 4), "unit": wl.unit, "cores": getattr(wl, "oracle_cores", 0) or oracle.num_threads(),
-                         "kind": "oracle", "sample": desc},
+        "cpu_baseline": {"value": round(value, 4), "unit": wl.unit,
+                         "cores": getattr(wl, "oracle_cores", 0) or oracle.num_threads(), "kind": "oracle",
+                         "sample": desc},
         "e2e": {"value": round(value, 4), "unit": wl.unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -1046,15 +1126,15 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
-    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5, 6, 7, 8, 9, 10])
+    ap.add_argument("--config", type=int, default=None, choices=[1, 2, 3, 4, 5, 6, 7, 8, 9, 10],
+                    help="one workload only (default: the headline decode B=128 L=32768 with the B=64 ragged "
+                         "decode and the T=8192 prefill calls as sub-records)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--graph", action="store_true",
                     help="capture each launch segment of the step as a CUDA graph and replay it")
     ap.add_argument("--budget-s", type=float, default=120.0,
                     help="reference arm: host seconds the whole --steps/--warmup run may take")
     args = ap.parse_args(argv)
-    if args.steps is None:
-        args.steps = DEFAULT_STEPS[args.config]
     args.warmup = max(3, args.warmup)
     world, rank, local = dist_info()
     if args.impl == "reference":

@@ -60,3 +60,26 @@ def test_reference_arm_under_torchrun_rank0_only():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["unit"] == "GB/s" and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_reference_arm_does_not_load_the_library():
+    """The reference arm times the oracle alone: the CUDA package is never
+    imported and libsinkattn.so is never mapped; its `config` names the
+    workload with the same keys as the native arm's line."""
+    code = (
+        "import io, json, os, sys, contextlib\n"
+        "sys.path.insert(0, %r)\n"
+        "import bench\n"
+        "buf = io.StringIO()\n"
+        "with contextlib.redirect_stdout(buf):\n"
+        "    bench.main(['--impl', 'reference', '--config', '1', '--steps', '2', '--warmup', '3', '--budget-s', '3'])\n"
+        "maps = open('/proc/self/maps').read()\n"
+        "print(json.dumps({'line': json.loads(buf.getvalue().strip().splitlines()[-1]),\n"
+        "                  'pkg': 'gqa_attention_sinks_head_gb300' in sys.modules,\n"
+        "                  'so': 'libsinkattn.so' in maps}))\n" % ROOT)
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    assert not d["pkg"] and not d["so"]
+    assert d["line"]["impl"] == "reference"
+    assert sorted(d["line"]["config"]) == ["global_batch", "parallelism", "seq_len_max", "workload"]
