@@ -554,10 +554,14 @@ sa_status_t prefill_impl(const void *q, bool q8, float q_scale, const int32_t *c
         return fail(SA_ERR_UNSUPPORTED, "E4M3 queries need an FP8-E4M3 cache");
     if (q8 && (!std::isfinite(q_scale) || q_scale == 0.f))
         return fail(SA_ERR_INVALID_ARG, "q_scale must be finite and nonzero");
-    st = encode_kv_map(&tk, kv->k, fp8, kv, 16, &dt, &dh, &dp);
+    // bf16: one box per 64-key tile when no tile straddles a page (contiguous
+    // sequences, or pages holding a multiple of 64 keys); else 16-key boxes
+    const int box_rows =
+        (!fp8 && ((!kv->page_table && kv->page_size >= 64) || kv->page_size % 64 == 0)) ? 64 : 16;
+    st = encode_kv_map(&tk, kv->k, fp8, kv, box_rows, &dt, &dh, &dp);
     if (st != SA_OK)
         return st;
-    st = encode_kv_map(&tv, kv->v, fp8, kv, 16, &dt, &dh, &dp);
+    st = encode_kv_map(&tv, kv->v, fp8, kv, box_rows, &dt, &dh, &dp);
     if (st != SA_OK)
         return st;
     {
@@ -602,6 +606,7 @@ sa_status_t prefill_impl(const void *q, bool q8, float q_scale, const int32_t *c
     p.max_kv_len = max_kv_len;
     p.window = window;
     p.num_q_tiles = (max_q_len + 127) / 128;
+    p.box_rows = box_rows;
     p.dim_token = dt;
     p.dim_head = dh;
     p.dim_page = dp;

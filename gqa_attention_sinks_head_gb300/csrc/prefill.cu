@@ -109,6 +109,25 @@ struct PrefillSmem {
 static_assert(sizeof(PrefillSmem<false>) + 1024 <= 113 * 1024, "two blocks must fit one SM's shared memory");
 static_assert(sizeof(PrefillSmem<true>) + 1024 <= 113 * 1024, "two blocks must fit one SM's shared memory");
 
+// Are all three phases complete?  One asm statement, so that the three
+// barrier reads overlap (about the latency of one); used as a fast path before
+// the bounded waits.
+__device__ __forceinline__ bool mbar_try_wait3(uint64_t *a, uint32_t pa, uint64_t *b, uint32_t pb, uint64_t *c,
+                                               uint32_t pc)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p, q, r;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %4;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 q, [%2], %5;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 r, [%3], %6;\n\t"
+        "and.pred p, p, q;\n\tand.pred p, p, r;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(a)), "r"(smem_u32(b)), "r"(smem_u32(c)), "r"(pa), "r"(pb), "r"(pc)
+        : "memory");
+    return ok != 0;
+}
+
 // bf16 pair -> f16 pair (round to nearest; |x| < 65504 assumed).
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t x)
 {
@@ -371,31 +390,42 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
             }
         } else {
-            int next_page = page_of(0);
+            // One box per lane, so that the copies' issue latencies overlap:
+            // lanes 0-3 the tile's K boxes, lanes 4-7 its V boxes (a 64-key box
+            // when no tile straddles a page: lanes 0 and 4).  A stage is refilled
+            // once the products that read its previous tile u have completed:
+            // Q K^T of tile u + 1 for the last head is issued behind every head's
+            // P V of tile u, so its S barrier says so (no commit of its own).
+            // Its phases are waited in order: a parity wait only looks one
+            // phase ahead.
+            const int is_v = (lane >> 2) & 1, bi = lane & 3;
+            const uint32_t box_bytes = static_cast<uint32_t>(p.box_rows) * kHeadDim * 2;
+            int seen = 0;  // phases of the last head's S barrier waited (phase k: Q K^T of tile k)
             for (int it = 0; it < ntiles; ++it) {
                 const int stage = it % kStages;
-                const int page = next_page;
-                const int nbox = boxes(it);
-                next_page = page_of(it + 1);  // one tile ahead: the table read overlaps the wait
-                if (it >= kStages && !mbar_wait(&sm.kv_empty[stage], ((it / kStages) - 1) & 1, p.status))
+                const int nbox = p.box_rows == 64 ? 1 : boxes(it);
+                bool ready = true;
+                for (; ready && it >= kStages && seen <= it - kStages + 1; ++seen)
+                    ready = mbar_wait(&sm.s_full[NH - 1], seen & 1, p.status);
+                if (!ready)
                     break;
-                const int key = (j_first + it) * BN + 16 * lane;
+                const int key = (j_first + it) * BN + 16 * bi;
+                const bool mine = lane < 8 && bi < nbox;
                 int c1 = 0, c2 = 0, c3 = 0;
-                if (lane < nbox) {
+                if (mine) {
+                    const int page = trow ? __ldg(trow + key / p.page_size) : b;
                     if (page < 0 || page >= p.num_pages)
                         atomicOr(p.status, SA_DEVICE_BAD_PAGE);  // outside the map: the box reads zeros
                     kv_coords(p, key % p.page_size, g, page, c1, c2, c3);
                 }
-                if (lane == 0)
-                    mbar_arrive_expect_tx(&sm.k_full[stage], static_cast<uint32_t>(nbox) * kBoxBytes);
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&sm.k_full[stage], static_cast<uint32_t>(nbox) * box_bytes);
+                    mbar_arrive_expect_tx(&sm.v_full[stage], static_cast<uint32_t>(nbox) * box_bytes);
+                }
                 __syncwarp();
-                if (lane < nbox)
-                    tma_load_4d(sm.k[stage] + lane * kBoxBytes, &tmk, &sm.k_full[stage], 0, c1, c2, c3);
-                if (lane == 0)
-                    mbar_arrive_expect_tx(&sm.v_full[stage], static_cast<uint32_t>(nbox) * kBoxBytes);
-                __syncwarp();
-                if (lane < nbox)
-                    tma_load_4d(sm.v[stage] + lane * kBoxBytes, &tmv, &sm.v_full[stage], 0, c1, c2, c3);
+                if (mine)
+                    tma_load_4d((is_v ? sm.v[stage] : sm.k[stage]) + bi * kBoxBytes, is_v ? &tmv : &tmk,
+                                is_v ? &sm.v_full[stage] : &sm.k_full[stage], 0, c1, c2, c3);
             }
         }
     } else if (warp == 1) {
@@ -451,7 +481,15 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         for (int it = 0; ok && it < ntiles; ++it) {
             const int stage = it % kStages;
-            if (!mbar_wait(&sm.v_full[stage], (it / kStages) & 1, p.status)) {
+            // bf16: V of this tile, P of head 0 and K of the next tile, checked
+            // together first; the bounded waits below only when one is missing
+            bool ready = false;
+            if constexpr (!FP8) {
+                const int kn = it + 1 < ntiles ? it + 1 : it;
+                ready = mbar_try_wait3(&sm.v_full[stage], (it / kStages) & 1, &sm.p_full[0], it & 1,
+                                       &sm.k_full[kn % kStages], (kn / kStages) & 1);
+            }
+            if (!ready && !mbar_wait(&sm.v_full[stage], (it / kStages) & 1, p.status)) {
                 ok = false;
                 break;
             }
@@ -467,7 +505,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 __syncwarp();
             }
             for (int t = 0; t < NH; ++t) {
-                if (!mbar_wait(&sm.p_full[t], it & 1, p.status)) {
+                if (!(ready && t == 0) && !mbar_wait(&sm.p_full[t], it & 1, p.status)) {
                     ok = false;
                     break;
                 }
@@ -475,7 +513,9 @@ __global__ void __launch_bounds__(kThreads, 2)
                 if (lane == 0)
                     issue_pv(t, stage, it > 0);
                 if (it + 1 < ntiles) {
-                    if (!wait_k(it + 1)) {
+                    // (bf16: after head 0 the next K is known to be there)
+                    const bool k_known = !FP8 && (ready || t > 0);
+                    if (!k_known && !wait_k(it + 1)) {
                         ok = false;
                         break;
                     }
@@ -488,7 +528,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                 __syncwarp();
             }
             if (lane == 0) {
-                umma_commit(&sm.kv_empty[stage]);
+                if (FP8)  // (bf16: the producer watches the last head's S barrier instead)
+                    umma_commit(&sm.kv_empty[stage]);
                 if (Q8 && ok && it + 1 < ntiles)
                     umma_commit(&sm.k8_empty[(it + 1) % kStaged]);  // every head's QK(it + 1) is issued
             }
