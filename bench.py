@@ -293,12 +293,14 @@ class DecodeBench:
     With sa=None (the reference arm) only the inputs are built: the same
     seeded bytes, drawn on the same device, and no library call is made."""
 
-    def __init__(self, sa, cfg, device):
+    def __init__(self, sa, cfg, device, batch=None):
         import torch
         import workloads as W
         self.sa, self.cfg, self.torch = sa, cfg, torch
         gen_dev = device if cfg in (2, 4, 5) else "cpu"
-        self.case = W.make_config(cfg, window=0, device=gen_dev).to(device)
+        self.case = W.make_config(cfg, window=0, device=gen_dev, batch=batch).to(device)
+        if batch is not None:
+            self.label = "%s; first %d sequences" % (workload_name(cfg), len(self.case.seqlens))
         self.sample_units = len(self.case.seqlens)
         c = self.case
         self.B, self.Hq, self.D = c.q.shape
@@ -669,7 +671,9 @@ class RopeBench:
         return dt, nbytes, "%d of %d tokens, every head" % (n, self.T)
 
 
-def make_bench(sa, cfg, device):
+def make_bench(sa, cfg, device, batch=None):
+    if batch is not None and cfg in (2, 4, 5):
+        return DecodeBench(sa, cfg, device, batch=batch)
     if cfg in ROPE_CONFIGS:
         return RopeBench(sa, cfg, device)
     if cfg in PREFILL_CONFIGS:
@@ -1033,7 +1037,7 @@ def run_native(args, world, rank, local):
     if args.config is not None:  # one workload
         cfg = args.config
         steps = args.steps if args.steps is not None else DEFAULT_STEPS[cfg]
-        rec = measure(make_bench(sa, cfg, "cuda"), cfg, args, world, rank, stream, sampler, steps, 10.0)
+        rec = measure(make_bench(sa, cfg, "cuda", args.batch), cfg, args, world, rank, stream, sampler, steps, 10.0)
         subs = {}
     else:
         # The default line: decode B=128, L=32768 (split-KV) as the headline;
@@ -1129,6 +1133,8 @@ def main(argv=None):
     ap.add_argument("--config", type=int, default=None, choices=[1, 2, 3, 4, 5, 6, 7, 8, 9, 10],
                     help="one workload only (default: the headline decode B=128 L=32768 with the B=64 ragged "
                          "decode and the T=8192 prefill calls as sub-records)")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="with --config 2, 4 or 5: only the first N sequences (a smaller case, e.g. for a profiler)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--graph", action="store_true",
                     help="capture each launch segment of the step as a CUDA graph and replay it")

@@ -265,7 +265,7 @@ def config_seqlens(cfg: int):
     raise ValueError(cfg)
 
 
-def make_config(cfg: int, *, window: int = 0, device="cpu") -> Case:
+def make_config(cfg: int, *, window: int = 0, device="cpu", batch: int | None = None) -> Case:
     """The five gpt-oss-shaped workloads (64 q / 8 kv heads, head_dim 64).
 
     1: decode, B=1, L=256, contiguous bf16, full causal.
@@ -280,8 +280,16 @@ def make_config(cfg: int, *, window: int = 0, device="cpu") -> Case:
     7: workload 6 on an FP8-E4M3 cache (per-tensor scales).
     8: multi-token decode: the cache of workload 2 (B=64, L_b ~ U[1024, 8192],
        paged bf16) with 4 new query tokens per sequence at L_b - 4 .. L_b - 1.
+
+    batch: decode workloads (2, 4, 5) only, keep the first `batch` sequences
+    (a smaller case of the same shape, e.g. for a profiler capture).
     """
     seed = CONFIG_SEED + cfg
+    if batch is not None and cfg in (2, 4, 5):
+        kl = config_seqlens(cfg)[:max(1, int(batch))]
+        return make_decode_case(kl, page_size=16, paged=True, window=window, poison_pages=64 if cfg == 2 else 0,
+                                kv_dtype="e4m3" if cfg == 5 else "bf16", seed=seed, device=device,
+                                name="config %d, first %d sequences w=%d" % (cfg, len(kl), window))
     if cfg == 1:
         return make_decode_case([256], page_size=256, paged=False, window=window, seed=seed,
                                 device=device, name="decode B=1 L=256 contiguous bf16")
