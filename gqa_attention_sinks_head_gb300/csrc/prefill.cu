@@ -102,7 +102,7 @@ struct PrefillSmem {
     uint64_t v_full[kStages];
     uint64_t kv_empty[kStages];
     uint64_t s_full[2];
-    uint64_t p_full[2];
+    uint64_t p_full[2][kStages];  // per head and ring stage: P of the stage's tile is in TMEM
     uint64_t o_done[2];
     uint32_t tmem_base;
 };
@@ -327,7 +327,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(&sm.s_full[t], 1);
-            mbar_init(&sm.p_full[t], 4);
+            for (int i = 0; i < kStages; ++i)
+                mbar_init(&sm.p_full[t][i], 4);
             mbar_init(&sm.o_done[t], 1);
         }
         fence_barrier_init();
@@ -395,25 +396,33 @@ __global__ void __launch_bounds__(kThreads, 2)
             // when no tile straddles a page: lanes 0 and 4).  A stage is refilled
             // once the products that read its previous tile u have completed:
             // Q K^T of tile u + 1 for the last head is issued behind every head's
-            // P V of tile u, so its S barrier says so (no commit of its own).
-            // Its phases are waited in order: a parity wait only looks one
-            // phase ahead.
+            // P V of tile u, and the softmax of that head's S of tile u + 1 has
+            // read it, so the last head's P barrier of tile u + 1 says so (no
+            // commit of its own).  The P barriers are per ring stage: the next
+            // phase of the one waited here needs a tile not yet loaded, so the
+            // parity wait cannot mistake a phase two ahead for the awaited one.
             const int is_v = (lane >> 2) & 1, bi = lane & 3;
             const uint32_t box_bytes = static_cast<uint32_t>(p.box_rows) * kHeadDim * 2;
-            int seen = 0;  // phases of the last head's S barrier waited (phase k: Q K^T of tile k)
+            auto nbox_of = [&](int it) { return p.box_rows == 64 ? 1 : boxes(it); };
+            auto page_for = [&](int it) -> int {  // the page of this lane's box of tile it
+                if (it >= ntiles || lane >= 8 || bi >= nbox_of(it))
+                    return 0;
+                const int key = (j_first + it) * BN + 16 * bi;
+                return trow ? __ldg(trow + key / p.page_size) : b;
+            };
+            int next_page = page_for(0);
             for (int it = 0; it < ntiles; ++it) {
                 const int stage = it % kStages;
-                const int nbox = p.box_rows == 64 ? 1 : boxes(it);
-                bool ready = true;
-                for (; ready && it >= kStages && seen <= it - kStages + 1; ++seen)
-                    ready = mbar_wait(&sm.s_full[NH - 1], seen & 1, p.status);
-                if (!ready)
+                const int nbox = nbox_of(it);
+                const int page = next_page;
+                next_page = page_for(it + 1);  // one tile ahead: the table read overlaps the wait
+                const int u1 = it - kStages + 1;  // the tile after the stage's previous one
+                if (u1 > 0 && !mbar_wait(&sm.p_full[NH - 1][u1 % kStages], (u1 / kStages) & 1, p.status))
                     break;
                 const int key = (j_first + it) * BN + 16 * bi;
                 const bool mine = lane < 8 && bi < nbox;
                 int c1 = 0, c2 = 0, c3 = 0;
                 if (mine) {
-                    const int page = trow ? __ldg(trow + key / p.page_size) : b;
                     if (page < 0 || page >= p.num_pages)
                         atomicOr(p.status, SA_DEVICE_BAD_PAGE);  // outside the map: the box reads zeros
                     kv_coords(p, key % p.page_size, g, page, c1, c2, c3);
@@ -486,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             bool ready = false;
             if constexpr (!FP8) {
                 const int kn = it + 1 < ntiles ? it + 1 : it;
-                ready = mbar_try_wait3(&sm.v_full[stage], (it / kStages) & 1, &sm.p_full[0], it & 1,
+                ready = mbar_try_wait3(&sm.v_full[stage], (it / kStages) & 1, &sm.p_full[0][stage], (it / kStages) & 1,
                                        &sm.k_full[kn % kStages], (kn / kStages) & 1);
             }
             if (!ready && !mbar_wait(&sm.v_full[stage], (it / kStages) & 1, p.status)) {
@@ -505,7 +514,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 __syncwarp();
             }
             for (int t = 0; t < NH; ++t) {
-                if (!(ready && t == 0) && !mbar_wait(&sm.p_full[t], it & 1, p.status)) {
+                if (!(ready && t == 0) && !mbar_wait(&sm.p_full[t][stage], (it / kStages) & 1, p.status)) {
                     ok = false;
                     break;
                 }
@@ -528,7 +537,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 __syncwarp();
             }
             if (lane == 0) {
-                if (FP8)  // (bf16: the producer watches the last head's S barrier instead)
+                if (FP8)  // (bf16: the producer watches the last head's P barriers instead)
                     umma_commit(&sm.kv_empty[stage]);
                 if (Q8 && ok && it + 1 < ntiles)
                     umma_commit(&sm.k8_empty[(it + 1) % kStaged]);  // every head's QK(it + 1) is issued
@@ -623,7 +632,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             tc_fence_before();
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(&sm.p_full[t]);
+                mbar_arrive(&sm.p_full[t][it % kStages]);
             if constexpr (FP8)  // the tile two ahead, while the tensor pipe runs PV and the next QK
                 if (it + kStages - 1 < ntiles)
                     ok = widen(it + kStages - 1);
