@@ -471,7 +471,11 @@ class MultiDecodeBench:
         self.elem = 1 if c.kv.dtype == "e4m3" else 2
         self.calls = []
         for w in windows_of(cfg):
-            S = sa.sa_decode_num_splits(self.B, self.Hkv, self.maxlen, w)
+            if sa is None:  # the reference arm: inputs only
+                self.calls.append(dict(window=w, S=1, bytes=multi_bytes(self.seqlens, w, self.q_len, self.Hkv,
+                                                                        self.Hq, self.D, self.elem)))
+                continue
+            S = sa.sa_decode_multi_num_splits(self.B, self.q_len, self.Hkv, self.maxlen, w, c.kv.dtype)
             nbytes = sa.sa_decode_multi_workspace_size(self.B, self.q_len, self.Hq, self.Hkv, self.D, self.maxlen,
                                                        w, S)
             self.calls.append(dict(

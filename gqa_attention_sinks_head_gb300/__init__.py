@@ -16,7 +16,8 @@ import os
 __all__ = [
     "SinkAttnError", "KVDesc", "load", "build", "sa_decode", "sa_decode_partial", "sa_merge_states",
     "sa_prefill", "sa_decode_static_workspace", "sa_decode_num_splits", "sa_decode_workspace_size", "sa_device_status", "sa_version",
-    "sa_decode_multi", "sa_decode_multi_workspace_size", "SA_MAX_DECODE_TOKENS", "sa_rope_yarn_table",
+    "sa_decode_multi", "sa_decode_multi_workspace_size", "sa_decode_multi_num_splits", "SA_MAX_DECODE_TOKENS",
+    "sa_rope_yarn_table",
     "sa_rope_append", "sa_prefill_q8", "sa_selftest_wait_timeout",
     "SA_KV_BF16", "SA_KV_FP8_E4M3", "kv_desc",
 ]
@@ -31,7 +32,8 @@ SA_DEVICE_SEQLEN_RANGE, SA_DEVICE_BAD_PAGE, SA_DEVICE_TIMEOUT, SA_DEVICE_BAD_QLE
 EXPORTS = ["sa_decode", "sa_decode_num_splits", "sa_decode_workspace_size", "sa_decode_partial",
            "sa_merge_states", "sa_prefill", "sa_device_status", "sa_status_string", "sa_last_error",
            "sa_version", "sa_decode_static_workspace", "sa_decode_multi", "sa_decode_multi_workspace_size",
-           "sa_rope_yarn_table", "sa_rope_append", "sa_prefill_q8", "sa_selftest_wait_timeout"]
+           "sa_decode_multi_num_splits", "sa_rope_yarn_table", "sa_rope_append", "sa_prefill_q8",
+           "sa_selftest_wait_timeout"]
 SA_MAX_DECODE_TOKENS = 8
 SA_STATIC_WORKSPACE_BYTES = 16 << 20
 
@@ -81,6 +83,8 @@ def load(path: str | None = None):
     lib.sa_decode_multi.argtypes = [P, i32, KP, P, i32, i32, i32, P, i32, f32, P, P, P, sz, i32, P]
     lib.sa_decode_multi_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32]
     lib.sa_decode_multi_workspace_size.restype = sz
+    lib.sa_decode_multi_num_splits.argtypes = [i32, i32, i32, i32, i32, i32]
+    lib.sa_decode_multi_num_splits.restype = i32
     dbl = ctypes.c_double
     lib.sa_rope_yarn_table.argtypes = [P, i32, i32, dbl, dbl, i32, dbl, dbl]
     lib.sa_rope_append.argtypes = [P, P, P, i32, i32, P, P, P, i32, KP, i32, P, f32, P]
@@ -185,6 +189,13 @@ def sa_decode_multi(q, q_len, kv, seqlens, sinks, window, sm_scale, out, lse=Non
                                _ptr(sinks), int(window), float(sm_scale), _ptr(out), _ptr(lse), _ptr(workspace),
                                ws_bytes, int(num_splits), _stream(stream)))
     return out, lse
+
+
+def sa_decode_multi_num_splits(batch, q_len, num_kv_heads, max_kv_len, window, kv_dtype="bf16") -> int:
+    """Chunk count of sa_decode_multi with num_splits = 0 (kv_dtype: "bf16" or "e4m3")."""
+    code = SA_KV_BF16 if kv_dtype == "bf16" else SA_KV_FP8_E4M3
+    return int(load().sa_decode_multi_num_splits(int(batch), int(q_len), int(num_kv_heads), int(max_kv_len),
+                                                 int(window), code))
 
 
 def sa_decode_multi_workspace_size(batch, q_len, num_qo_heads, num_kv_heads, head_dim, max_kv_len, window,

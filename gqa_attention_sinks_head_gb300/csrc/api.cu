@@ -43,7 +43,7 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 uint32_t *g_status_ptr[kMaxDevices] = {nullptr};
 int g_sm_count[kMaxDevices] = {0};
-int g_bps[2][kMaxDevices] = {{0}};  // decode blocks per SM (bf16, fp8)
+int g_bps[3][kMaxDevices] = {{0}};  // blocks per SM: decode bf16, decode fp8, multi-token tcgen05
 
 cudaError_t status_ptr(uint32_t **out)
 {
@@ -65,8 +65,10 @@ cudaError_t status_ptr(uint32_t **out)
     return cudaSuccess;
 }
 
-// SM count and decode occupancy of the current device (cached).
-bool device_shape(bool fp8, int *sms, int *bps)
+// SM count and the occupancy of a decode kernel (kind: 0 the one-token bf16
+// kernel, 1 its FP8 build, 2 the multi-token tcgen05 kernel) on the current
+// device (cached).
+bool device_shape(int kind, int *sms, int *bps)
 {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
@@ -82,16 +84,17 @@ bool device_shape(bool fp8, int *sms, int *bps)
         }
         g_sm_count[dev] = n;
     }
-    if (!g_bps[fp8][dev]) {
+    if (!g_bps[kind][dev]) {
         int b = 0;
-        if (sa::decode_occupancy(fp8, &b) != cudaSuccess || b <= 0) {
+        const cudaError_t e = kind == 2 ? sa::decode_mt_occupancy(&b) : sa::decode_occupancy(kind == 1, &b);
+        if (e != cudaSuccess || b <= 0) {
             cudaGetLastError();
             b = 1;
         }
-        g_bps[fp8][dev] = b;
+        g_bps[kind][dev] = b;
     }
     *sms = g_sm_count[dev];
-    *bps = g_bps[fp8][dev];
+    *bps = g_bps[kind][dev];
     return true;
 }
 
@@ -329,6 +332,30 @@ sa_status_t launch_decode_kernel(const void *q, int32_t q_len, const sa_kv_desc_
     p.dim_page = dp;
     p.score_scale = sm_scale * kLog2e * (fp8 ? kv->k_scale : 1.f);  // FP8: codes widen to their values
     p.out_scale = fp8 ? kv->v_scale : 1.f;
+    if (q_len > 1 && !fp8 && q_len * p.group <= 64) {
+        // several tokens on a bf16 cache: the tcgen05 kernel, whose Q tile is
+        // one TMA box of the group's heads x the sequence's q_len tokens
+        EncodeTiledFn fn = encode_fn();
+        if (!fn)
+            return fail(SA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+        CUtensorMap tq;
+        const cuuint64_t dims[3] = {static_cast<cuuint64_t>(sa::kHeadDim), static_cast<cuuint64_t>(num_qo_heads),
+                                    static_cast<cuuint64_t>(batch) * static_cast<cuuint64_t>(q_len)};
+        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(sa::kHeadDim) * 2,
+                                       static_cast<cuuint64_t>(num_qo_heads) * sa::kHeadDim * 2};
+        const cuuint32_t box[3] = {static_cast<cuuint32_t>(sa::kHeadDim), static_cast<cuuint32_t>(p.group),
+                                   static_cast<cuuint32_t>(q_len)};
+        const cuuint32_t estr[3] = {1, 1, 1};
+        CUresult r = fn(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(q), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS)
+            return fail(SA_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled rejected q (CUresult %d)", (int)r);
+        e = sa::launch_decode_mt(tq, tk, tv, p, stream);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "multi-token decode launch");
+        return SA_OK;
+    }
     e = sa::launch_decode(tk, tv, p, fp8, stream);
     if (e != cudaSuccess)
         return cuda_fail(e, "decode launch");
@@ -368,9 +395,22 @@ int sa_version(void) { return SA_VERSION; }
 int32_t sa_decode_num_splits(int32_t batch, int32_t num_kv_heads, int32_t max_kv_len, int32_t window)
 {
     int sms = 0, bps = 0;
-    if (!device_shape(false, &sms, &bps)) {
+    if (!device_shape(0, &sms, &bps)) {
         sms = 152;  // no device visible: size for a GB300
         bps = 4;
+    }
+    return choose_splits(batch, std::max(1, num_kv_heads), max_kv_len, window, sms, bps);
+}
+
+int32_t sa_decode_multi_num_splits(int32_t batch, int32_t q_len, int32_t num_kv_heads, int32_t max_kv_len,
+                                   int32_t window, int32_t kv_dtype)
+{
+    if (q_len <= 1 || kv_dtype != SA_KV_BF16)  // the one-token kernel's blocks
+        return sa_decode_num_splits(batch, num_kv_heads, max_kv_len, window);
+    int sms = 0, bps = 0;
+    if (!device_shape(2, &sms, &bps)) {
+        sms = 152;
+        bps = 2;
     }
     return choose_splits(batch, std::max(1, num_kv_heads), max_kv_len, window, sms, bps);
 }
@@ -411,8 +451,8 @@ sa_status_t decode_impl(const void *q, int32_t q_len, const sa_kv_desc_t *kv, co
     if (batch == 0)
         return SA_OK;
     const int32_t rows = batch * q_len;
-    const int32_t S =
-        num_splits == 0 ? sa_decode_num_splits(batch, kv->num_kv_heads, max_kv_len, window) : num_splits;
+    const int32_t S = num_splits != 0 ? num_splits
+                      : sa_decode_multi_num_splits(batch, q_len, kv->num_kv_heads, max_kv_len, window, kv->dtype);
     if (S <= 1)
         return launch_decode_kernel(q, q_len, kv, seqlens, batch, num_qo_heads, max_kv_len, sinks, window,
                                     sm_scale, out, lse, nullptr, nullptr, 1, false, stream);
@@ -451,7 +491,12 @@ size_t sa_decode_multi_workspace_size(int32_t batch, int32_t q_len, int32_t num_
 {
     if (batch <= 0 || q_len <= 0 || num_qo_heads <= 0 || head_dim <= 0 || num_splits < 0)
         return 0;
-    const int32_t S = num_splits == 0 ? sa_decode_num_splits(batch, num_kv_heads, max_kv_len, window) : num_splits;
+    // (num_splits = 0: enough for the automatic choice on either cache type)
+    const int32_t S =
+        num_splits != 0
+            ? num_splits
+            : std::max(sa_decode_multi_num_splits(batch, q_len, num_kv_heads, max_kv_len, window, SA_KV_BF16),
+                       sa_decode_multi_num_splits(batch, q_len, num_kv_heads, max_kv_len, window, SA_KV_FP8_E4M3));
     return S <= 1 ? 0 : partial_bytes(S, batch * q_len, num_qo_heads, head_dim);
 }
 

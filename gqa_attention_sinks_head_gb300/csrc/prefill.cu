@@ -58,6 +58,7 @@
 
 #include "sa_internal.h"
 #include "sa_ptx.cuh"
+#include "tmem_softmax.cuh"
 
 namespace sa {
 namespace {
@@ -76,13 +77,16 @@ __host__ __device__ constexpr uint32_t col_s(int t) { return 128u * t; }        
 __host__ __device__ constexpr uint32_t col_o(int t) { return 128u * t + 64u; }  // O_t
 constexpr float kLog2e = 1.44269504088896340736f;
 constexpr float kLn2 = 0.69314718055994530942f;
-constexpr float kRescaleThreshold = 8.0f;  // log2 of the largest tolerated p
 // Q, K both K-major; V is MN-major (dims contiguous).  f16 operands for an FP8 cache.
 template <bool FP8>
 constexpr uint32_t kIdescQK = idesc_f32acc(BM, BN, 0, FP8);
 constexpr uint32_t kIdescQK8 = idesc_e4m3_f32acc(BM, BN);  // E4M3 Q and K
 template <bool FP8>
 constexpr uint32_t kIdescPV = idesc_f32acc(BM, kHeadDim, 1, FP8);
+
+using tsm::mask_tile;
+using tsm::softmax_tile;
+static_assert(BN == tsm::kCols, "the softmax helpers take 64-key tiles");
 
 template <bool FP8>
 struct PrefillSmem {
@@ -163,104 +167,6 @@ __device__ __forceinline__ void kv_coords(const PrefillParams &p, int slot, int 
     c1 = p.dim_token == 1 ? slot : (p.dim_head == 1 ? g : page);
     c2 = p.dim_token == 2 ? slot : (p.dim_head == 2 ? g : page);
     c3 = p.dim_token == 3 ? slot : (p.dim_head == 3 ? g : page);
-}
-
-// Edge tiles (straddling the causal diagonal, the window's lower edge or the
-// sequence end): overwrite the hidden keys' scores in TMEM with -inf, by
-// select, so that NaN scores past the sequence vanish too.  The row sees the
-// tile's columns lo .. hi (none when hi < lo).  A 32-column chunk that every
-// row of the warp sees whole is skipped.  Interior tiles skip this and the
-// softmax body carries no mask arithmetic.
-__device__ __forceinline__ void mask_tile(uint32_t s_addr, int lo, int hi)
-{
-    // column e is visible iff (unsigned)(e - lo) <= span
-    const uint32_t span = hi >= lo ? static_cast<uint32_t>(hi - lo) : 0u;
-    const int lo_eff = hi >= lo ? lo : (1 << 20);
-#pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
-        if (__all_sync(0xffffffffu, lo <= 32 * c && hi >= 32 * c + 31))
-            continue;
-        uint32_t v[32];
-        tmem_ld32(s_addr + 32 * c, v);
-        tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-            v[i] = static_cast<uint32_t>(32 * c + i - lo_eff) <= span ? v[i] : 0xff800000u;
-        tmem_st32(s_addr + 32 * c, v);
-    }
-    tmem_st_wait();
-}
-
-// One 64-key tile of the online softmax for the query row this thread owns.
-// Pass 1 reads S (TMEM) 16 columns at a time for the row max; pass 2 reads it
-// again, forms p = 2^(s*scale - m) (fma.f32x2, ex2; ex2 of -inf is exactly 0),
-// adds p into two paired sums (add.f32x2), packs p to bf16 and stores it as P
-// over the leading columns of S.  When m moved, O is rescaled.
-template <bool FP8>
-__device__ __forceinline__ void softmax_tile(uint32_t s_addr, uint32_t o_addr, float scale, bool o_live, float &m,
-                                             float &l)
-{
-    constexpr int kChunk = 16;  // columns per TMEM read: few live registers at two blocks per SM
-    uint32_t sr[kChunk];
-    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-    for (int c = 0; c < BN / kChunk; ++c) {
-        tmem_ld16(s_addr + kChunk * c, sr);
-        tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < kChunk; i += 8)
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4)
-                mx[q4] = max3f(mx[q4], __uint_as_float(sr[i + 2 * q4]), __uint_as_float(sr[i + 2 * q4 + 1]));
-    }
-    const float mt = max3f(mx[0], mx[1], fmaxf(mx[2], mx[3])) * scale;  // scale > 0
-    const bool upd = mt > m + kRescaleThreshold;
-    const bool any_upd = __any_sync(0xffffffffu, upd);
-    float alpha = 1.f;
-    if (upd) {
-        alpha = ex2(m - mt);  // m = -inf gives 0
-        l *= alpha;
-        m = mt;
-    }
-    const float negmu = m == -INFINITY ? 0.f : -m;
-    const uint64_t scale2 = f2_pack(scale, scale);
-    const uint64_t negmu2 = f2_pack(negmu, negmu);
-    uint64_t ls2[2] = {0ull, 0ull};
-#pragma unroll
-    for (int c = 0; c < BN / kChunk; ++c) {
-        tmem_ld16(s_addr + kChunk * c, sr);
-        tmem_ld_wait();
-        uint32_t pk[kChunk / 2];
-#pragma unroll
-        for (int i = 0; i < kChunk; i += 2) {
-            float x0, x1;
-            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[i]), __uint_as_float(sr[i + 1])), scale2, negmu2), x0, x1);
-            const float p0 = ex2(x0);
-            const float p1 = ex2(x1);
-            ls2[(i >> 1) & 1] = f2_add(ls2[(i >> 1) & 1], f2_pack(p0, p1));
-            pk[i >> 1] = FP8 ? pack_f16(p0, p1) : pack_bf16(p0, p1);
-        }
-        tmem_st8(s_addr + (kChunk / 2) * c, pk);  // P columns [8c, 8c+8): S columns already read
-    }
-    float a0, a1, b0, b1;
-    f2_unpack(ls2[0], a0, a1);
-    f2_unpack(ls2[1], b0, b1);
-    l += (a0 + a1) + (b0 + b1);
-    if (any_upd && o_live) {
-        // O holds earlier tiles at the old max: rescale it.  PV of this tile
-        // waits for the P handshake, and PV of the previous tile completed
-        // before this S was reported.
-#pragma unroll
-        for (int c = 0; c < kHeadDim / 32; ++c) {
-            uint32_t ov[32];
-            tmem_ld32(o_addr + 32 * c, ov);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-                ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-            tmem_st32(o_addr + 32 * c, ov);
-        }
-    }
 }
 
 template <bool FP8, bool Q8>

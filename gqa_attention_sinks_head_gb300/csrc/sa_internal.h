@@ -133,6 +133,11 @@ cudaError_t once_per_device(std::atomic<int> (&flags)[kMaxDevices], F &&set)
 cudaError_t launch_decode(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p,
                           bool fp8, cudaStream_t stream);
 cudaError_t decode_occupancy(bool fp8, int *blocks_per_sm);
+// bf16 cache, q_len 2..8: tq maps q as [B * q_len, Hq, 64] with a box of
+// (64, group, q_len); tk / tv take 16-key boxes
+cudaError_t launch_decode_mt(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                             const DecodeParams &p, cudaStream_t stream);
+cudaError_t decode_mt_occupancy(int *blocks_per_sm);
 cudaError_t launch_merge(const MergeParams &p, cudaStream_t stream);
 cudaError_t launch_rope_append(const RopeParams &p, cudaStream_t stream);
 cudaError_t launch_wait_timeout_selftest(uint32_t *status, cudaStream_t stream);

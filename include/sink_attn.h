@@ -188,7 +188,10 @@ size_t sa_decode_workspace_size(int32_t batch, int32_t num_qo_heads, int32_t num
  *   out, lse   device bf16 [batch * q_len, num_qo_heads, 64] / fp32
  *              [batch * q_len, num_qo_heads] or NULL, rows as q
  *   workspace  at least sa_decode_multi_workspace_size(...) bytes when split
+ *   num_splits 0 = sa_decode_multi_num_splits(...); otherwise as sa_decode
  *   other arguments as sa_decode; q_len = 1 is sa_decode.
+ * q_len >= 2 on a bf16 cache runs on the tensor cores (tcgen05): the group's
+ * q_len x G query rows against 64-key tiles, two key streams per block.
  * A sequence with 0 < seqlens[b] < q_len sets SA_DEVICE_BAD_QLEN; its tokens
  * at negative positions see no key (out = 0, lse = sink).  seqlens[b] = 0
  * marks an empty slot: every token of it gives out = 0, lse = sink, unflagged.
@@ -203,8 +206,19 @@ sa_status_t sa_decode_multi(const void *q, int32_t q_len, const sa_kv_desc_t *kv
                             size_t workspace_bytes, int32_t num_splits, cudaStream_t stream);
 
 /*
- * Workspace bytes sa_decode_multi needs (the chunk count is that of
- * sa_decode_num_splits for num_splits = 0).  Layout when S > 1: fp32 o_part
+ * Number of KV chunks sa_decode_multi uses for num_splits = 0 on the current
+ * device, for a cache of type kv_dtype (an sa_kv_dtype_t).  q_len >= 2 on a
+ * bf16 cache runs the tensor-core multi-token kernel (two blocks per SM, so
+ * fewer chunks fill the GPU); otherwise this is sa_decode_num_splits.  Depends
+ * only on the arguments and the device (no device sync).
+ */
+int32_t sa_decode_multi_num_splits(int32_t batch, int32_t q_len, int32_t num_kv_heads,
+                                   int32_t max_kv_len, int32_t window, int32_t kv_dtype);
+
+/*
+ * Workspace bytes sa_decode_multi needs.  num_splits = 0 gives a size that
+ * covers the automatic choice for either cache type (the larger of the two
+ * sa_decode_multi_num_splits counts).  Layout when S > 1: fp32 o_part
  * [S, batch * q_len, num_qo_heads, head_dim] followed (at a 256-byte aligned
  * offset) by fp32 lse_part [S, batch * q_len, num_qo_heads].
  */

@@ -152,6 +152,23 @@ def test_decode_multi_validation_matches_decode(lib):
     assert _decode_multi(lib, _desc(lib), 4, batch=0, q=None, seqlens=None, out=None) == 0
 
 
+def test_multi_token_split_count(lib):
+    """sa_decode_multi_num_splits: the one-token count for q_len 1 and for FP8
+    caches; for q_len >= 2 on bf16 the tensor-core kernel (two blocks per SM)
+    takes no more chunks; the automatic workspace covers either choice."""
+    L = lib.load()
+    for B, Hkv, Lmax, w in [(64, 8, 8192, 0), (1, 8, 32768, 0), (4, 8, 4096, 0), (256, 8, 8192, 128), (1, 1, 1, 0)]:
+        one = L.sa_decode_num_splits(B, Hkv, Lmax, w)
+        assert L.sa_decode_multi_num_splits(B, 1, Hkv, Lmax, w, lib.SA_KV_BF16) == one
+        for q_len in (2, 4, 8):
+            assert L.sa_decode_multi_num_splits(B, q_len, Hkv, Lmax, w, lib.SA_KV_FP8_E4M3) == one
+            s = L.sa_decode_multi_num_splits(B, q_len, Hkv, Lmax, w, lib.SA_KV_BF16)
+            assert 1 <= s <= one
+            auto = L.sa_decode_multi_workspace_size(B, q_len, 64, Hkv, 64, Lmax, w, 0)
+            assert auto == L.sa_decode_multi_workspace_size(B, q_len, 64, Hkv, 64, Lmax, w, max(s, one))
+    assert L.sa_decode_multi_num_splits(1, 4, 8, 32768, 0, lib.SA_KV_BF16) > 4  # one long sequence is spread out
+
+
 def test_decode_multi_workspace_size(lib):
     assert lib.sa_decode_multi_workspace_size(4, 3, 64, 8, 64, 1000, 0, 1) == 0
     s = lib.sa_decode_multi_workspace_size(4, 3, 64, 8, 64, 1000, 0, 5)
