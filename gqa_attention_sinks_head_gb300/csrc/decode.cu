@@ -71,6 +71,7 @@ struct DecodeCfg {
 };
 
 constexpr int kMaxTPW = 2;  // query tokens per consumer warp (q_len <= 8)
+constexpr int kMaxOrderedBatch = 128;  // batches up to this size run longest sequence first
 // Row stride (floats) of the block-merge scratch [slot][head][dim]: 4 floats of
 // padding put the 8 heads of a warp's float4 reads and of the fragment writes
 // in different banks.
@@ -85,6 +86,8 @@ struct DecodeSmem {
     float red_l[kConsumerWarps][kMaxTPW][kMaxGroup];
     uint64_t full[kStages];
     uint64_t empty[kStages];
+    int32_t seq;                     // the sequence this block serves
+    int32_t lens[kMaxOrderedBatch];  // scratch: the batch's lengths, for the ordering
 };
 
 // Byte offset of 16-byte chunk `chunk` of row `row` in a swizzled tile.
@@ -122,7 +125,29 @@ __global__ void __launch_bounds__(kThreads, TPW == 1 ? 4 : (kJoint ? 2 : 3)) dec
     const int lane = threadIdx.x & 31;
     const int split = blockIdx.x;
     const int g = blockIdx.y;
-    const int b = blockIdx.z;
+    // Longest sequences first: block z serves the sequence of rank z in
+    // decreasing length (ties by index), so that the blocks of a ragged batch
+    // start longest first and no long one starts last (list scheduling,
+    // longest job first).  Only unsplit calls: split chunks are of equal
+    // length already, and a windowed call gives every sequence the same keys.
+    const bool ordered = p.batch <= kMaxOrderedBatch && p.window == 0 && p.num_splits == 1;
+    if (ordered) {
+        for (int i = threadIdx.x; i < p.batch; i += kThreads)
+            sm.lens[i] = __ldg(p.seqlens + i);
+        __syncthreads();
+        for (int i = threadIdx.x; i < p.batch; i += kThreads) {
+            const int li = sm.lens[i];
+            int rank = 0;
+            for (int k = 0; k < p.batch; ++k) {
+                const int lk = sm.lens[k];
+                rank += (lk > li || (lk == li && k < i)) ? 1 : 0;
+            }
+            if (rank == static_cast<int>(blockIdx.z))
+                sm.seq = i;
+        }
+        __syncthreads();
+    }
+    const int b = ordered ? sm.seq : static_cast<int>(blockIdx.z);
 
     // ---- the block's key range: the union over its query tokens -----------
     const int qlen = p.q_len;

@@ -55,6 +55,8 @@
 // sink enters the denominator once.
 #include <cuda_bf16.h>
 
+#include <algorithm>
+
 #include "sa_internal.h"
 #include "sa_ptx.cuh"
 #include "tmem_softmax.cuh"
@@ -74,6 +76,7 @@ constexpr uint32_t kQBytes = kRows * kHeadDim * 2;      // 16 KB
 constexpr uint32_t kTileBytes = kKeys * kHeadDim * 2;   // 8 KB
 constexpr uint32_t kBoxBytes = 16 * kHeadDim * 2;       // one 16-key box
 constexpr uint32_t kTmemCols = 256;
+constexpr int kMaxOrderedBatch = 128;  // batches up to this size run longest sequence first
 constexpr float kLog2e = 1.44269504088896340736f;
 constexpr float kLn2 = 0.69314718055994530942f;
 // Q, K K-major; V MN-major (dims contiguous); bf16 operands, fp32 accumulators
@@ -93,6 +96,8 @@ struct MtSmem {
     uint64_t p_full[2];          // per stream: P of its current tile is in TMEM
     uint64_t o_done;             // every product has completed
     uint32_t tmem_base;
+    int32_t seq;                       // the sequence this block serves
+    int32_t lens[kMaxOrderedBatch];    // scratch: the batch's lengths, for the ordering
 };
 constexpr size_t kSmemBytes = sizeof(MtSmem) + 1024;  // + slack for the 1 KB alignment
 static_assert(2 * (kSmemBytes + 1024) <= 228 * 1024, "two blocks must fit one SM's shared memory");
@@ -119,7 +124,30 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int lane = threadIdx.x & 31;
     const int split = blockIdx.x;
     const int g = blockIdx.y;
-    const int b = blockIdx.z;
+    // Longest sequences first: block z serves the sequence of rank z in
+    // decreasing length (ties by index).  The blocks of a ragged batch then
+    // start in that order, so no long one starts last and runs alone at the
+    // end (list scheduling, longest job first).  Only unsplit calls: split
+    // chunks are of equal length already, and a windowed call gives every
+    // sequence the same keys.
+    const bool ordered = p.batch <= kMaxOrderedBatch && p.window == 0 && p.num_splits == 1;
+    if (ordered) {
+        for (int i = threadIdx.x; i < p.batch; i += kThreads)
+            sm.lens[i] = __ldg(p.seqlens + i);
+        __syncthreads();
+        for (int i = threadIdx.x; i < p.batch; i += kThreads) {
+            const int li = sm.lens[i];
+            int rank = 0;
+            for (int k = 0; k < p.batch; ++k) {
+                const int lk = sm.lens[k];
+                rank += (lk > li || (lk == li && k < i)) ? 1 : 0;
+            }
+            if (rank == static_cast<int>(blockIdx.z))
+                sm.seq = i;
+        }
+        __syncthreads();
+    }
+    const int b = ordered ? sm.seq : static_cast<int>(blockIdx.z);
     const int qlen = p.q_len;
     const int G = p.group;
     const int R = qlen * G;            // live rows of the tile
@@ -339,9 +367,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                 break;
             tc_fence_after();
             const int key0 = t_begin + j * kKeys;
-            if (__any_sync(0xffffffffu, vlo > key0 || vhi < key0 + kKeys))
-                tsm::mask_tile(s_addr, vlo - key0, vhi - 1 - key0);
-            tsm::softmax_tile<false>(s_addr, o_addr, p.score_scale, j >= 2, m, l);
+            const bool edge = __any_sync(0xffffffffu, vlo > key0 || vhi < key0 + kKeys);
+            tsm::softmax_tile_r<false>(s_addr, o_addr, p.score_scale, j >= 2, edge, vlo - key0, vhi - 1 - key0, m, l);
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
@@ -465,12 +492,21 @@ cudaError_t prepare_decode_mt()
 
 }  // namespace
 
+// Blocks per SM: the launch bounds reserve registers for two, so shared
+// memory decides (two blocks resident, as measured on GB300;
+// cudaOccupancyMaxActiveBlocksPerMultiprocessor reports one for this kernel).
 cudaError_t decode_mt_occupancy(int *blocks_per_sm)
 {
-    const cudaError_t e = prepare_decode_mt();
+    int dev = 0, smem_sm = 0, reserved = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
     if (e != cudaSuccess)
         return e;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, decode_mt_kernel, kThreads, kSmemBytes);
+    *blocks_per_sm = std::min(2, smem_sm / static_cast<int>(kSmemBytes + reserved));
+    return cudaSuccess;
 }
 
 cudaError_t launch_decode_mt(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,

@@ -112,5 +112,81 @@ __device__ __forceinline__ void softmax_tile(uint32_t s_addr, uint32_t o_addr, f
 }
 
 
+// softmax_tile with the row's 64 scores held in registers: one TMEM read of S
+// (two 32-column loads, one wait), the edge mask applied by select (column e
+// is visible iff lo <= e <= hi; `edge` false skips it), the max, the p pass
+// and one 32-column store of P.  Two TMEM round trips per tile instead of
+// eight, for kernels whose softmax sits on the critical chain and can spare
+// the registers.
+template <bool FP8>
+__device__ __forceinline__ void softmax_tile_r(uint32_t s_addr, uint32_t o_addr, float scale, bool o_live, bool edge,
+                                               int lo, int hi, float &m, float &l)
+{
+    uint32_t sa[32], sb[32];
+    tmem_ld32(s_addr, sa);
+    tmem_ld32(s_addr + 32, sb);
+    tmem_ld_wait();
+    if (edge) {
+        const uint32_t span = hi >= lo ? static_cast<uint32_t>(hi - lo) : 0u;
+        const int lo_eff = hi >= lo ? lo : (1 << 20);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            sa[i] = static_cast<uint32_t>(i - lo_eff) <= span ? sa[i] : 0xff800000u;
+            sb[i] = static_cast<uint32_t>(32 + i - lo_eff) <= span ? sb[i] : 0xff800000u;
+        }
+    }
+    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+    for (int i = 0; i < 32; i += 4) {
+        mx[0] = max3f(mx[0], __uint_as_float(sa[i]), __uint_as_float(sa[i + 1]));
+        mx[1] = max3f(mx[1], __uint_as_float(sa[i + 2]), __uint_as_float(sa[i + 3]));
+        mx[2] = max3f(mx[2], __uint_as_float(sb[i]), __uint_as_float(sb[i + 1]));
+        mx[3] = max3f(mx[3], __uint_as_float(sb[i + 2]), __uint_as_float(sb[i + 3]));
+    }
+    const float mt = max3f(mx[0], mx[1], fmaxf(mx[2], mx[3])) * scale;  // scale > 0
+    const bool upd = mt > m + kRescaleThreshold;
+    const bool any_upd = __any_sync(0xffffffffu, upd);
+    float alpha = 1.f;
+    if (upd) {
+        alpha = ex2(m - mt);  // m = -inf gives 0
+        l *= alpha;
+        m = mt;
+    }
+    const float negmu = m == -INFINITY ? 0.f : -m;
+    const uint64_t scale2 = f2_pack(scale, scale);
+    const uint64_t negmu2 = f2_pack(negmu, negmu);
+    uint64_t ls2[2] = {0ull, 0ull};
+    uint32_t pk[32];
+#pragma unroll
+    for (int i = 0; i < 64; i += 2) {
+        const uint32_t *src = i < 32 ? sa + i : sb + (i - 32);
+        float x0, x1;
+        f2_unpack(f2_fma(f2_pack(__uint_as_float(src[0]), __uint_as_float(src[1])), scale2, negmu2), x0, x1);
+        const float p0 = ex2(x0);
+        const float p1 = ex2(x1);
+        ls2[(i >> 1) & 1] = f2_add(ls2[(i >> 1) & 1], f2_pack(p0, p1));
+        pk[i >> 1] = FP8 ? pack_f16(p0, p1) : pack_bf16(p0, p1);
+    }
+    tmem_st32(s_addr, pk);  // P over S columns 0 .. 31 (all of S is in registers)
+    float a0, a1, b0, b1;
+    f2_unpack(ls2[0], a0, a1);
+    f2_unpack(ls2[1], b0, b1);
+    l += (a0 + a1) + (b0 + b1);
+    if (any_upd && o_live) {
+        // O holds earlier tiles at the old max: rescale it (PV of the
+        // previous tile completed before this S was reported)
+#pragma unroll
+        for (int c = 0; c < kHeadDim / 32; ++c) {
+            uint32_t ov[32];
+            tmem_ld32(o_addr + 32 * c, ov);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+            tmem_st32(o_addr + 32 * c, ov);
+        }
+    }
+}
+
 }  // namespace tsm
 }  // namespace sa
