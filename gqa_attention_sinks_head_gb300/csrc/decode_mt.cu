@@ -317,8 +317,11 @@ __global__ void __launch_bounds__(kThreads, 2)
         // round j: P V(j) and Q K^T(j + 2), both from step j + 2
         for (int j = 0; ok && j < ntiles; ++j) {
             const int s = j & 1, i = j + 2, stage = i % kStages;
-            if (!mbar_wait(&sm.p_full[s], (j >> 1) & 1, p.status) ||
-                !mbar_wait(&sm.full[stage], (i / kStages) & 1, p.status)) {
+            // P(j) and step i, checked together first; the bounded waits only
+            // when one is missing
+            const bool ready = mbar_try_wait2(&sm.p_full[s], (j >> 1) & 1, &sm.full[stage], (i / kStages) & 1);
+            if (!ready && (!mbar_wait(&sm.p_full[s], (j >> 1) & 1, p.status) ||
+                           !mbar_wait(&sm.full[stage], (i / kStages) & 1, p.status))) {
                 ok = false;
                 break;
             }

@@ -113,25 +113,6 @@ struct PrefillSmem {
 static_assert(sizeof(PrefillSmem<false>) + 1024 <= 113 * 1024, "two blocks must fit one SM's shared memory");
 static_assert(sizeof(PrefillSmem<true>) + 1024 <= 113 * 1024, "two blocks must fit one SM's shared memory");
 
-// Are all three phases complete?  One asm statement, so that the three
-// barrier reads overlap (about the latency of one); used as a fast path before
-// the bounded waits.
-__device__ __forceinline__ bool mbar_try_wait3(uint64_t *a, uint32_t pa, uint64_t *b, uint32_t pb, uint64_t *c,
-                                               uint32_t pc)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p, q, r;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %4;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 q, [%2], %5;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 r, [%3], %6;\n\t"
-        "and.pred p, p, q;\n\tand.pred p, p, r;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(a)), "r"(smem_u32(b)), "r"(smem_u32(c)), "r"(pa), "r"(pb), "r"(pc)
-        : "memory");
-    return ok != 0;
-}
-
 // bf16 pair -> f16 pair (round to nearest; |x| < 65504 assumed).
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t x)
 {

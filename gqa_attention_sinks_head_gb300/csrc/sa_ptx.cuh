@@ -79,6 +79,41 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t pari
     return ok != 0;
 }
 
+// Are all three phases complete?  One asm statement, so that the three
+// barrier reads overlap (about the latency of one); used as a fast path before
+// the bounded waits.
+__device__ __forceinline__ bool mbar_try_wait3(uint64_t *a, uint32_t pa, uint64_t *b, uint32_t pb, uint64_t *c,
+                                               uint32_t pc)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p, q, r;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %4;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 q, [%2], %5;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 r, [%3], %6;\n\t"
+        "and.pred p, p, q;\n\tand.pred p, p, r;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(a)), "r"(smem_u32(b)), "r"(smem_u32(c)), "r"(pa), "r"(pb), "r"(pc)
+        : "memory");
+    return ok != 0;
+}
+
+// Are both phases complete?  One asm statement, so that the two barrier
+// reads overlap; a fast path before the bounded waits.
+__device__ __forceinline__ bool mbar_try_wait2(uint64_t *a, uint32_t pa, uint64_t *b, uint32_t pb)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %3;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 q, [%2], %4;\n\t"
+        "and.pred p, p, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(a)), "r"(smem_u32(b)), "r"(pa), "r"(pb)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for the phase with the given parity to complete.  Returns false when
 // the wait ran out its time limit, or when it has lasted over a millisecond and
 // another block already recorded a timeout (the status word then holds
