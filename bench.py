@@ -511,7 +511,10 @@ class MultiDecodeBench:
             self.run_call(cl, stream, None if evs is None else evs[i])
 
     def dominant(self):
-        return 0, "decode_kernel (with its merge)", self.calls[0]["bytes"]
+        # q_len >= 2 on a bf16 cache runs the tcgen05 kernel (an FP8 cache the
+        # one-token kernel's multi-token build); a split call adds the merge
+        name = "decode_mt_kernel" if self.elem == 2 and self.q_len > 1 else "decode_kernel"
+        return 0, name + (" (with its merge)" if self.calls[0]["S"] > 1 else ""), self.calls[0]["bytes"]
 
     def segment_names(self):
         return ["decode q_len=%d w=%d (%d chunks)" % (self.q_len, cl["window"], cl["S"]) for cl in self.calls]
