@@ -8,7 +8,10 @@
 //   out = sum_s exp(lse_s - M) o_s / Z,  lse = M + log Z.
 // One warp per (n, h): the lanes first take the max of the S log-sum-exps,
 // then each lane accumulates a float4 slice of the head dimension over the
-// chunks (reads are float4-coalesced across the warp).
+// chunks (reads are float4-coalesced across the warp).  For head_dim 64 and
+// up to 16 chunks the two half-warps take alternate chunks, and every load
+// (the log-sum-exps and all value slices) is issued before any is used: one
+// memory round trip instead of two.
 #include <cuda_bf16.h>
 
 #include "sa_internal.h"
@@ -35,6 +38,53 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergePara
     const float sigma = p.sinks ? __ldg(p.sinks + h) : -INFINITY;
     const int S = p.num_splits;
     const int D = p.head_dim;
+    __nv_bfloat16 *out = reinterpret_cast<__nv_bfloat16 *>(p.out) + row * D;
+
+    if (D == 64 && S <= 16) {
+        const int half = lane >> 4, d = 4 * (lane & 15);  // chunks half, half + 2, ..; dims d .. d + 3
+        float4 v[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int s = half + 2 * k;
+            v[k] = s < S ? __ldg(reinterpret_cast<const float4 *>(p.o_part + (s * NH + row) * 64 + d))
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        const float ls = lane < S ? __ldg(p.lse_part + lane * NH + row) : -INFINITY;
+        float M = fmaxf(sigma, ls);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+            M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        if (M == -INFINITY) {  // no key anywhere and no sink
+            if (lane < 16)
+                *reinterpret_cast<uint2 *>(out + d) = make_uint2(0u, 0u);
+            if (lane == 0 && p.lse_out)
+                p.lse_out[row] = -INFINITY;
+            return;
+        }
+        const float w_lane = ls == -INFINITY ? 0.f : expf(ls - M);  // lane s: chunk s's weight
+        float Z = w_lane;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+            Z += __shfl_xor_sync(0xffffffffu, Z, off);
+        Z += sigma == -INFINITY ? 0.f : expf(sigma - M);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const float w = __shfl_sync(0xffffffffu, w_lane, (half + 2 * k) & 31);  // 0 past S
+            acc.x += w * v[k].x, acc.y += w * v[k].y, acc.z += w * v[k].z, acc.w += w * v[k].w;
+        }
+        acc.x += __shfl_xor_sync(0xffffffffu, acc.x, 16);  // the two halves' chunks
+        acc.y += __shfl_xor_sync(0xffffffffu, acc.y, 16);
+        acc.z += __shfl_xor_sync(0xffffffffu, acc.z, 16);
+        acc.w += __shfl_xor_sync(0xffffffffu, acc.w, 16);
+        const float inv = 1.f / Z;
+        if (lane < 16)
+            *reinterpret_cast<uint2 *>(out + d) =
+                make_uint2(pack_bf16(acc.x * inv, acc.y * inv), pack_bf16(acc.z * inv, acc.w * inv));
+        if (lane == 0 && p.lse_out)
+            p.lse_out[row] = M + logf(Z);
+        return;
+    }
 
     // lane s holds lse of chunk s (chunks past 32 fold in below)
     float ls = lane < S ? __ldg(p.lse_part + lane * NH + row) : -INFINITY;
@@ -45,7 +95,6 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergePara
     for (int off = 16; off > 0; off >>= 1)
         M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
 
-    __nv_bfloat16 *out = reinterpret_cast<__nv_bfloat16 *>(p.out) + row * D;
     if (M == -INFINITY) {  // no key anywhere and no sink
         for (int d = 4 * lane; d < D; d += 128)
             *reinterpret_cast<uint2 *>(out + d) = make_uint2(0u, 0u);
