@@ -736,6 +736,10 @@ class PrefillBench:
                                             " + ".join("w=%d" % w for w in windows))
         self.B = len(self.q_lens)
         self.maxlen = max(self.kv_lens)
+        if self.streamed_e2e():
+            self.e2e_api = ("sa_prefill from pinned host q, k, v, streamed in 4 query chunks (chunk i's rows in on a "
+                            "copy stream, its calls for those queries against keys up to its last position, its "
+                            "out/lse back on a third stream)")
         # algorithmic bytes of a call: q in, out and lse back, and the K/V rows
         # some query of the call sees (a window call is bound by these, not by flops)
         qe = 1 if self.q8 else 2
@@ -808,10 +812,13 @@ class PrefillBench:
 
     def e2e(self, stream, steps, warmup, flush=None):
         """Per step: one copy of q (or its codes), k and v in, the calls, one
-        copy of every call's out and lse back."""
+        copy of every call's out and lse back.  A single contiguous sequence
+        streams instead (e2e_streamed)."""
         import dataclasses
         torch = self.torch
         c = self.case
+        if self.streamed_e2e():
+            return self.e2e_streamed(stream, steps, warmup, flush)
         inp = Packed(torch, [self.q_codes if self.q8 else c.q, c.kv.k, c.kv.v])
         q = inp.dev[0]
         kv = dataclasses.replace(c.kv, k=inp.dev[1], v=inp.dev[2])
@@ -825,6 +832,76 @@ class PrefillBench:
 
         ms = timed_loop(torch, stream, one, steps, warmup, flush)
         return ms, inp.nbytes, res.nbytes
+
+    def streamed_e2e(self):
+        c = self.case
+        return self.B == 1 and c.kv.page_table is None and c.kv.layout == "NHD" and not self.q8 and self.T % 4 == 0
+
+    def e2e_streamed(self, stream, steps, warmup, flush=None, chunks=4):
+        """One sequence from pinned host memory, in `chunks` query chunks: the
+        rows of chunk i (its q, and the k and v of its positions) go in on a
+        copy stream; on the compute stream each call runs for the chunk's
+        queries against the keys up to its last position (chunked prefill:
+        the same rows, positions and flops as the whole call); the chunk's out
+        and lse come back on a third stream.  Later chunks' copies overlap
+        earlier chunks' calls.  Every input byte goes in and every result byte
+        comes back once per step."""
+        import dataclasses
+        torch = self.torch
+        c = self.case
+        T, Tc = self.T, self.T // chunks
+        k, v = c.kv.k, c.kv.v  # [1, page, Hkv, D]: token-major rows of one sequence
+        hq = c.q.cpu().pin_memory()
+        hk, hv = k.cpu().pin_memory(), v.cpu().pin_memory()
+        dq, dk, dv = torch.empty_like(c.q), torch.empty_like(k), torch.empty_like(v)
+        kv = dataclasses.replace(c.kv, k=dk, v=dv)
+        res = [(torch.empty_like(cl["out"]), torch.empty_like(cl["lse"])) for cl in self.calls]
+        hres = [(torch.empty(o.shape, dtype=o.dtype, pin_memory=True), torch.empty(l.shape, dtype=l.dtype, pin_memory=True))
+                for o, l in res]
+        cu = torch.tensor([0, Tc], dtype=torch.int32, device="cuda")
+        kv_len = [torch.tensor([(i + 1) * Tc], dtype=torch.int32, device="cuda") for i in range(chunks)]
+        s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+
+        def one():
+            start = torch.cuda.Event()
+            start.record(stream)
+            s_in.wait_event(start)
+            s_out.wait_event(start)
+            landed = []
+            with torch.cuda.stream(s_in):
+                for i in range(chunks):
+                    r = slice(i * Tc, (i + 1) * Tc)
+                    dq[r].copy_(hq[r], non_blocking=True)
+                    dk[0, r].copy_(hk[0, r], non_blocking=True)
+                    dv[0, r].copy_(hv[0, r], non_blocking=True)
+                    e = torch.cuda.Event()
+                    e.record(s_in)
+                    landed.append(e)
+            done = []
+            for i in range(chunks):
+                r = slice(i * Tc, (i + 1) * Tc)
+                stream.wait_event(landed[i])
+                for cl, (o, l) in zip(self.calls, res):
+                    self.sa.sa_prefill(dq[r], cu, kv, kv_len[i], c.sinks, cl["window"], c.sm_scale, o[r], l[r],
+                                       max_q_len=Tc, max_kv_len=(i + 1) * Tc, stream=stream)
+                e = torch.cuda.Event()
+                e.record(stream)
+                done.append(e)
+            with torch.cuda.stream(s_out):
+                for i in range(chunks):
+                    r = slice(i * Tc, (i + 1) * Tc)
+                    s_out.wait_event(done[i])
+                    for (o, l), (ho, hl) in zip(res, hres):
+                        ho[r].copy_(o[r], non_blocking=True)
+                        hl[r].copy_(l[r], non_blocking=True)
+            end = torch.cuda.Event()
+            end.record(s_out)
+            stream.wait_event(end)
+
+        ms = timed_loop(torch, stream, one, steps, warmup, flush)
+        h2d = (c.q.numel() + 2 * T * self.Hkv * self.D) * 2
+        d2h = sum(o.numel() * o.element_size() + l.numel() * l.element_size() for o, l in res)
+        return ms, h2d, d2h
 
     def oracle_sample(self, budget_s, max_seqs=None):
         """Rows of the sequence, all heads: the first, then every k-th."""
