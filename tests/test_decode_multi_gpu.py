@@ -121,3 +121,34 @@ def test_config8_full_size(sa, oracle, window):
     rows = np.concatenate([np.arange(4 * s, 4 * s + 4) for s in seqs]).astype(np.int32)
     ref_o, ref_l = oracle_prefill(oracle, case, rows)
     check_close(out[rows], lse[rows], ref_o, ref_l, "config 8 w=%d" % window)
+
+
+@pytest.mark.parametrize("splits", [1, 3])
+def test_cuda_graph_capture_and_replay(sa, oracle, splits):
+    """The tcgen05 multi-token call (its Q tensor map encoded per call, held by
+    value in the launch) captured into a CUDA graph and replayed after the
+    output was overwritten; split and unsplit (longest-first) forms."""
+    q_len = 4
+    case = case_of(q_len, [100, 900, 2000, 37], seed=460)
+    cg = case.to("cuda")
+    R, Hq, D = cg.q.shape
+    B = cg.seqlens.shape[0]
+    out = torch.empty(R, Hq, D, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(R, Hq, device="cuda")
+    ws = torch.empty(max(sa.sa_decode_multi_workspace_size(B, q_len, Hq, 8, D, 2000, 0, splits), 16),
+                     dtype=torch.uint8, device="cuda")
+    run = lambda: sa.sa_decode_multi(cg.q, q_len, cg.kv, cg.seqlens, cg.sinks, 0, cg.sm_scale, out, lse,
+                                     max_kv_len=2000, workspace=ws, num_splits=splits)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        run()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        run()
+    out.fill_(float("nan"))
+    graph.replay()
+    torch.cuda.synchronize()
+    ref_o, ref_l = oracle_prefill(oracle, case)
+    check_close(out, lse, ref_o, ref_l, "multi-token graph replay S=%d" % splits)
+    assert sa.sa_device_status() == 0
