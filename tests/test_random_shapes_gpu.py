@@ -57,6 +57,24 @@ def test_random_multi_token_decode(sa, oracle, seed):
 
 
 @pytest.mark.parametrize("seed", range(8))
+def test_random_multi_token_decode_bf16(sa, oracle, seed):
+    """bf16 caches (the tensor-core multi-token kernel), batches up to past
+    the 128 sequences that the unsplit call orders longest first."""
+    g, hq, hkv, page, layout, _, window = _draw(8000 + seed)
+    q_len = int(g.integers(2, 9))
+    B = int(g.choice([1, 7, 64, 129]))
+    lens = [int(x) for x in g.choice([q_len, q_len + 1, 64, 100, 513, 2000], B)]
+    splits = int(g.choice([0, 1, 3]))
+    case = W.make_prefill_case([q_len] * len(lens), lens, num_qo_heads=hq, num_kv_heads=hkv, paged=True,
+                               page_size=page, layout=layout, window=window, poison_pages=2, seed=9000 + seed)
+    out, lse = multi_gpu(sa, case.to("cuda"), q_len, splits)
+    ref_o, ref_l = oracle_prefill(oracle, case)
+    check_close(out, lse, ref_o, ref_l, "random bf16 multi-token decode %d: q_len=%d B=%d %s w=%d P=%d Hq/Hkv=%d/%d "
+                "S=%d" % (seed, q_len, B, layout, window, page, hq, hkv, splits))
+    assert sa.sa_device_status() == 0
+
+
+@pytest.mark.parametrize("seed", range(8))
 def test_random_prefill(sa, oracle, seed):
     g, hq, hkv, page, layout, kv_dtype, window = _draw(5000 + seed)
     kv_lens = [int(x) for x in g.choice([1, 64, 129, 300, 700], int(g.integers(1, 4)))]
