@@ -529,23 +529,38 @@ __global__ void __launch_bounds__(kThreads, 2)
             tc_fence_after();
             const float inv = l > 0.f ? (FP8 ? p.out_scale : 1.f) / l : 0.f;
             const int64_t orow = static_cast<int64_t>(q_beg + qi) * p.num_qo_heads + h;
-            uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.out) + orow * kHeadDim);
+            // The warp's 32 rows of O, in bf16, go through this head's Q tile
+            // (every product that read it has completed) so that the global
+            // stores are whole 128-byte rows: chunk c of row r sits at chunk
+            // c ^ (r & 7), which keeps both the row-wise writes and the
+            // chunk-wise reads free of bank conflicts.
+            uint8_t *stage_o = sm.q[t] + quarter * 32 * 128;
 #pragma unroll
             for (int c = 0; c < kHeadDim / 32; ++c) {  // 32 columns of O at a time
                 uint32_t ov[32];
                 tmem_ld32(o_addr + 32 * c, ov);
                 tmem_ld_wait();
-                if (qi < Lq) {
 #pragma unroll
-                    for (int v4 = 0; v4 < 4; ++v4) {
-                        uint4 w;
-                        w.x = pack_bf16(__uint_as_float(ov[8 * v4 + 0]) * inv, __uint_as_float(ov[8 * v4 + 1]) * inv);
-                        w.y = pack_bf16(__uint_as_float(ov[8 * v4 + 2]) * inv, __uint_as_float(ov[8 * v4 + 3]) * inv);
-                        w.z = pack_bf16(__uint_as_float(ov[8 * v4 + 4]) * inv, __uint_as_float(ov[8 * v4 + 5]) * inv);
-                        w.w = pack_bf16(__uint_as_float(ov[8 * v4 + 6]) * inv, __uint_as_float(ov[8 * v4 + 7]) * inv);
-                        dst[c * 4 + v4] = w;
-                    }
+                for (int v4 = 0; v4 < 4; ++v4) {
+                    uint4 w;
+                    w.x = pack_bf16(__uint_as_float(ov[8 * v4 + 0]) * inv, __uint_as_float(ov[8 * v4 + 1]) * inv);
+                    w.y = pack_bf16(__uint_as_float(ov[8 * v4 + 2]) * inv, __uint_as_float(ov[8 * v4 + 3]) * inv);
+                    w.z = pack_bf16(__uint_as_float(ov[8 * v4 + 4]) * inv, __uint_as_float(ov[8 * v4 + 5]) * inv);
+                    w.w = pack_bf16(__uint_as_float(ov[8 * v4 + 6]) * inv, __uint_as_float(ov[8 * v4 + 7]) * inv);
+                    *reinterpret_cast<uint4 *>(stage_o + lane * 128 + (((4 * c + v4) ^ (lane & 7)) << 4)) = w;
                 }
+            }
+            __syncwarp();
+            // eight lanes per row, four rows per store
+            const int ch = lane & 7;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int r = 4 * i + (lane >> 3);
+                const int qr = q0 + quarter * 32 + r;
+                const uint4 w = *reinterpret_cast<const uint4 *>(stage_o + r * 128 + ((ch ^ (r & 7)) << 4));
+                if (qr < Lq)
+                    reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.out) +
+                                              (static_cast<int64_t>(q_beg + qr) * p.num_qo_heads + h) * kHeadDim)[ch] = w;
             }
             if (qi < Lq && p.lse)
                 p.lse[orow] = l > 0.f ? (m + lg2(l)) * kLn2 : -INFINITY;
