@@ -3,9 +3,10 @@
 // One thread block per (128-query tile, pair of query heads of one kv group,
 // sequence), two blocks per SM.  The two heads share every K/V tile: the block
 // streams 64-key tiles of K and V through a 4-stage shared-memory ring filled
-// by TMA (16-key boxes, so a paged cache needs no special case), and both
-// heads' products run on the 5th-generation tensor cores with their
-// accumulators in tensor memory (256 columns per block):
+// by TMA (16-key boxes, so a paged cache needs no special case; one 64-key box
+// per operand when no tile straddles a page), and both heads' products run on
+// the 5th-generation tensor cores with their accumulators in tensor memory
+// (256 columns per block):
 //
 //   TMEM columns   0..63   S_0 = Q_0 K^T (fp32), its first 32 columns reused for P_0 (bf16 pairs)
 //                 64..127  O_0 (fp32)
@@ -19,7 +20,8 @@
 //   warps 2-5   softmax of head 0, warps 6-9 softmax of head 1: one thread per query
 //               row; warp w reads TMEM lanes 32*(w%4) .. +31, so each group of four
 //               warps covers all 128 rows.  For an FP8 cache they also widen the
-//               staged codes to f16, two tiles ahead.
+//               staged codes to f16, two tiles ahead.  At the end each warp stages
+//               its 32 output rows in its head's Q tile and stores whole rows.
 //
 // Two blocks per SM give four independent softmax streams per SM, and one
 // block's prologue, tail and epilogue overlap the other block's work.  Per key
