@@ -505,6 +505,16 @@ __global__ void __launch_bounds__(kThreads, 2)
         if constexpr (FP8)
             for (int j = 0; ok && j < min(ntiles, kStages - 1); ++j)
                 ok = widen(j);
+        // The row's visible keys, and the tiles it_lo .. it_hi - 1 that every
+        // row of the block sees whole (the rest straddle the causal diagonal,
+        // the window's lower edge or the sequence end), worked out once so that
+        // the tile loop keeps two bounds live instead of the block's geometry.
+        const int row_lo = p.window > 0 ? max(pos - p.window + 1, 0) : 0;
+        const int row_hi = min(pos, Lkv - 1);
+        // below: every row sees the keys from p_last - window + 1 on (window > 0)
+        const int it_lo = p.window > 0 ? max(0, (p_last - p.window + BN) / BN - j_first) : 0;
+        // above: every row sees the keys below min(p_first + 1, Lkv)
+        const int it_hi = max(it_lo, min(p_first + 1, Lkv) / BN - j_first);
         for (int it = 0; ok && it < ntiles; ++it) {
             if (!mbar_wait(&sm.s_full[t], it & 1, p.status)) {
                 ok = false;
@@ -512,10 +522,8 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
             tc_fence_after();
             const int key0 = (j_first + it) * BN;
-            const bool edge =
-                key0 + BN - 1 > p_first || (p.window > 0 && key0 <= p_last - p.window) || key0 + BN > Lkv;
-            if (edge)  // this row sees keys max(pos - window + 1, 0) .. min(pos, Lkv - 1)
-                mask_tile(s_addr, (p.window > 0 ? max(pos - p.window + 1, 0) : 0) - key0, min(pos, Lkv - 1) - key0);
+            if (it < it_lo || it >= it_hi)  // an edge tile: this row sees keys row_lo .. row_hi
+                mask_tile(s_addr, row_lo - key0, row_hi - key0);
             softmax_tile<FP8>(s_addr, o_addr, p.score_scale, it > 0, m, l);  // (P in f16 for both FP8 modes)
             tmem_st_wait();
             tc_fence_before();
