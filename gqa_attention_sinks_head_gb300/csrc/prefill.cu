@@ -152,7 +152,11 @@ __device__ __forceinline__ void kv_coords(const PrefillParams &p, int slot, int 
     c3 = p.dim_token == 3 ? slot : (p.dim_head == 3 ? g : page);
 }
 
-template <bool FP8, bool Q8>
+// NH: query heads per block, 2 (a pair of one kv group) or 1 (odd groups).
+// A compile-time count lets the MMA warp's per-head loop unroll, with every
+// head's TMEM columns and barriers fixed, which shortens the P -> next S
+// round trip that bounds the kernel.
+template <bool FP8, bool Q8, int NH>
 __global__ void __launch_bounds__(kThreads, 2)
     prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                    const __grid_constant__ CUtensorMap tmv, const PrefillParams p)
@@ -169,7 +173,6 @@ __global__ void __launch_bounds__(kThreads, 2)
     griddep_launch_dependents();  // the next call's grid may be scheduled as this one drains
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int NH = p.heads_per_cta;
     const int h0 = blockIdx.x * NH;
     const int g = h0 / p.group;
     const int qt = static_cast<int>(gridDim.y) - 1 - static_cast<int>(blockIdx.y);  // heavy tiles first
@@ -592,19 +595,19 @@ size_t prefill_smem_bytes()
     return sizeof(PrefillSmem<FP8>) + 1024;  // + slack for the 1 KB alignment
 }
 
-template <bool FP8, bool Q8>
+template <bool FP8, bool Q8, int NH>
 cudaError_t launch_of(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv, const PrefillParams &p,
                       cudaStream_t stream)
 {
     static std::atomic<int> done[kMaxDevices];  // one cudaFuncSetAttribute per device and variant
     const cudaError_t e = once_per_device(done, [] {
-        return cudaFuncSetAttribute(prefill_kernel<FP8, Q8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        return cudaFuncSetAttribute(prefill_kernel<FP8, Q8, NH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(prefill_smem_bytes<FP8>()));
     });
     if (e != cudaSuccess)
         return e;
     const dim3 grid(p.num_qo_heads / p.heads_per_cta, p.num_q_tiles, p.batch);
-    return launch_pdl(prefill_kernel<FP8, Q8>, grid, dim3(kThreads), prefill_smem_bytes<FP8>(), stream, tq, tk, tv, p);
+    return launch_pdl(prefill_kernel<FP8, Q8, NH>, grid, dim3(kThreads), prefill_smem_bytes<FP8>(), stream, tq, tk, tv, p);
 }
 
 }  // namespace
@@ -612,9 +615,13 @@ cudaError_t launch_of(const CUtensorMap &tq, const CUtensorMap &tk, const CUtens
 cudaError_t launch_prefill(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                            const PrefillParams &p, bool fp8, bool q8, cudaStream_t stream)
 {
+    const bool pair = p.heads_per_cta == 2;
     if (q8)
-        return launch_of<true, true>(tq, tk, tv, p, stream);
-    return fp8 ? launch_of<true, false>(tq, tk, tv, p, stream) : launch_of<false, false>(tq, tk, tv, p, stream);
+        return pair ? launch_of<true, true, 2>(tq, tk, tv, p, stream) : launch_of<true, true, 1>(tq, tk, tv, p, stream);
+    if (fp8)
+        return pair ? launch_of<true, false, 2>(tq, tk, tv, p, stream)
+                    : launch_of<true, false, 1>(tq, tk, tv, p, stream);
+    return pair ? launch_of<false, false, 2>(tq, tk, tv, p, stream) : launch_of<false, false, 1>(tq, tk, tv, p, stream);
 }
 
 }  // namespace sa
