@@ -58,6 +58,8 @@
 // once the QK products that read it have completed.
 #include <cuda_bf16.h>
 
+#include <type_traits>
+
 #include "sa_internal.h"
 #include "sa_ptx.cuh"
 #include "tmem_softmax.cuh"
@@ -380,46 +382,47 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
             __syncwarp();
         }
-        for (int it = 0; ok && it < ntiles; ++it) {
+        // One key tile; LAST (compile time) marks the block's last tile, the
+        // only one with no next Q K^T and the only one that can reach past the
+        // sequence end, so the steady-state tiles carry neither test.
+        auto tile = [&](auto LAST_, int it) -> bool {
+            constexpr bool LAST = decltype(LAST_)::value;
             const int stage = it % kStages;
             // bf16: V of this tile, P of head 0 and K of the next tile, checked
             // together first; the bounded waits below only when one is missing
             bool ready = false;
             if constexpr (!FP8) {
-                const int kn = it + 1 < ntiles ? it + 1 : it;
+                const int kn = LAST ? it : it + 1;
                 ready = mbar_try_wait3(&sm.v_full[stage], (it / kStages) & 1, &sm.p_full[0][stage], (it / kStages) & 1,
                                        &sm.k_full[kn % kStages], (kn / kStages) & 1);
             }
-            if (!ready && !mbar_wait(&sm.v_full[stage], (it / kStages) & 1, p.status)) {
-                ok = false;
-                break;
-            }
-            const int key0 = (j_first + it) * BN;
-            if (!FP8 && key0 + BN > Lkv) {  // (the FP8 widening zeroes these rows itself)
-                // value rows past the sequence may hold anything (NaN included):
-                // zero them so that p = 0 contributes exactly 0
-                const int first_bad = max(Lkv - key0, 0);
-                uint4 *vz = reinterpret_cast<uint4 *>(sm.v[stage]);
-                for (int i = first_bad * 8 + lane; i < BN * 8; i += 32)
-                    vz[i] = make_uint4(0u, 0u, 0u, 0u);
-                fence_proxy_async_smem();
-                __syncwarp();
-            }
-            for (int t = 0; t < NH; ++t) {
-                if (!(ready && t == 0) && !mbar_wait(&sm.p_full[t][stage], (it / kStages) & 1, p.status)) {
-                    ok = false;
-                    break;
+            if (!ready && !mbar_wait(&sm.v_full[stage], (it / kStages) & 1, p.status))
+                return false;
+            if constexpr (!FP8 && LAST) {  // (the FP8 widening zeroes these rows itself)
+                const int key0 = (j_first + it) * BN;
+                if (key0 + BN > Lkv) {
+                    // value rows past the sequence may hold anything (NaN included):
+                    // zero them so that p = 0 contributes exactly 0
+                    const int first_bad = max(Lkv - key0, 0);
+                    uint4 *vz = reinterpret_cast<uint4 *>(sm.v[stage]);
+                    for (int i = first_bad * 8 + lane; i < BN * 8; i += 32)
+                        vz[i] = make_uint4(0u, 0u, 0u, 0u);
+                    fence_proxy_async_smem();
+                    __syncwarp();
                 }
+            }
+#pragma unroll
+            for (int t = 0; t < NH; ++t) {
+                if (!(ready && t == 0) && !mbar_wait(&sm.p_full[t][stage], (it / kStages) & 1, p.status))
+                    return false;
                 tc_fence_after();
                 if (lane == 0)
                     issue_pv(t, stage, it > 0);
-                if (it + 1 < ntiles) {
+                if constexpr (!LAST) {
                     // (bf16: after head 0 the next K is known to be there)
                     const bool k_known = !FP8 && (ready || t > 0);
-                    if (!k_known && !wait_k(it + 1)) {
-                        ok = false;
-                        break;
-                    }
+                    if (!k_known && !wait_k(it + 1))
+                        return false;
                     tc_fence_after();
                     if (lane == 0) {
                         issue_qk(t, k_slot(it + 1));
@@ -431,11 +434,16 @@ __global__ void __launch_bounds__(kThreads, 2)
             if (lane == 0) {
                 if (FP8)  // (bf16: the producer watches the last head's P barriers instead)
                     umma_commit(&sm.kv_empty[stage]);
-                if (Q8 && ok && it + 1 < ntiles)
+                if (Q8 && !LAST)
                     umma_commit(&sm.k8_empty[(it + 1) % kStaged]);  // every head's QK(it + 1) is issued
             }
             __syncwarp();
-        }
+            return true;
+        };
+        for (int it = 0; ok && it + 1 < ntiles; ++it)
+            ok = tile(std::false_type{}, it);
+        if (ok && ntiles > 0)
+            ok = tile(std::true_type{}, ntiles - 1);
         if (lane == 0)
             for (int t = 0; t < NH; ++t)
                 umma_commit(&sm.o_done[t]);
