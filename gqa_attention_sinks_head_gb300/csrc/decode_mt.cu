@@ -56,6 +56,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <type_traits>
 
 #include "sa_internal.h"
 #include "sa_ptx.cuh"
@@ -314,35 +315,43 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
             __syncwarp();
         }
-        // round j: P V(j) and Q K^T(j + 2), both from step j + 2
-        for (int j = 0; ok && j < ntiles; ++j) {
+        // round j: P V(j) and Q K^T(j + 2), both from step j + 2.  QK (compile
+        // time): there is a tile j + 2; TAIL: the round's tile may reach past the
+        // chunk (only the last one can).  The steady rounds carry neither test.
+        auto round = [&](auto QK_, auto TAIL_, int j) -> bool {
+            constexpr bool QK = decltype(QK_)::value, TAIL = decltype(TAIL_)::value;
             const int s = j & 1, i = j + 2, stage = i % kStages;
             // P(j) and step i, checked together first; the bounded waits only
             // when one is missing
             const bool ready = mbar_try_wait2(&sm.p_full[s], (j >> 1) & 1, &sm.full[stage], (i / kStages) & 1);
             if (!ready && (!mbar_wait(&sm.p_full[s], (j >> 1) & 1, p.status) ||
-                           !mbar_wait(&sm.full[stage], (i / kStages) & 1, p.status))) {
-                ok = false;
-                break;
-            }
-            const int key0 = t_begin + j * kKeys;
-            if (key0 + kKeys > t_end) {
-                // value rows past the chunk: zeros, so that p = 0 contributes exactly 0
-                uint4 *vz = reinterpret_cast<uint4 *>(sm.v[stage]);
-                for (int e = (t_end - key0) * (kHeadDim / 8) + lane; e < kKeys * (kHeadDim / 8); e += 32)
-                    vz[e] = make_uint4(0u, 0u, 0u, 0u);
-                fence_proxy_async_smem();
-                __syncwarp();
+                           !mbar_wait(&sm.full[stage], (i / kStages) & 1, p.status)))
+                return false;
+            if constexpr (TAIL) {
+                const int key0 = t_begin + j * kKeys;
+                if (key0 + kKeys > t_end) {
+                    // value rows past the chunk: zeros, so that p = 0 contributes exactly 0
+                    uint4 *vz = reinterpret_cast<uint4 *>(sm.v[stage]);
+                    for (int e = (t_end - key0) * (kHeadDim / 8) + lane; e < kKeys * (kHeadDim / 8); e += 32)
+                        vz[e] = make_uint4(0u, 0u, 0u, 0u);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                }
             }
             tc_fence_after();
             if (lane == 0) {
                 issue_pv(s, stage, j >= 2);
-                if (i < ntiles)
+                if constexpr (QK)
                     issue_qk(s, stage);
                 umma_commit(&sm.done[stage]);  // frees step i and reports S(i)
             }
             __syncwarp();
-        }
+            return true;
+        };
+        for (int j = 0; ok && j + 2 < ntiles; ++j)
+            ok = round(std::true_type{}, std::false_type{}, j);
+        for (int j = max(0, ntiles - 2); ok && j < ntiles; ++j)
+            ok = round(std::false_type{}, std::true_type{}, j);
         if (lane == 0)
             umma_commit(&sm.o_done);
         __syncwarp();
