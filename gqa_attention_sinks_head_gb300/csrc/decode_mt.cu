@@ -318,14 +318,18 @@ __global__ void __launch_bounds__(kThreads, 2)
         // round j: P V(j) and Q K^T(j + 2), both from step j + 2.  QK (compile
         // time): there is a tile j + 2; TAIL: the round's tile may reach past the
         // chunk (only the last one can).  The steady rounds carry neither test.
+        // ring stage and phase of step j + 2, advanced round by round (no
+        // division by the ring depth on the issue path)
+        int stage = 2 % kStages, sphase = 0;
         auto round = [&](auto QK_, auto TAIL_, int j) -> bool {
             constexpr bool QK = decltype(QK_)::value, TAIL = decltype(TAIL_)::value;
-            const int s = j & 1, i = j + 2, stage = i % kStages;
+            const int s = j & 1;
+            const uint32_t ph = static_cast<uint32_t>(sphase);
             // P(j) and step i, checked together first; the bounded waits only
             // when one is missing
-            const bool ready = mbar_try_wait2(&sm.p_full[s], (j >> 1) & 1, &sm.full[stage], (i / kStages) & 1);
+            const bool ready = mbar_try_wait2(&sm.p_full[s], (j >> 1) & 1, &sm.full[stage], ph);
             if (!ready && (!mbar_wait(&sm.p_full[s], (j >> 1) & 1, p.status) ||
-                           !mbar_wait(&sm.full[stage], (i / kStages) & 1, p.status)))
+                           !mbar_wait(&sm.full[stage], ph, p.status)))
                 return false;
             if constexpr (TAIL) {
                 const int key0 = t_begin + j * kKeys;
@@ -346,6 +350,10 @@ __global__ void __launch_bounds__(kThreads, 2)
                 umma_commit(&sm.done[stage]);  // frees step i and reports S(i)
             }
             __syncwarp();
+            if (++stage == kStages) {
+                stage = 0;
+                sphase ^= 1;
+            }
             return true;
         };
         for (int j = 0; ok && j + 2 < ntiles; ++j)
