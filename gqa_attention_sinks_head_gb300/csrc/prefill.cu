@@ -388,13 +388,16 @@ __global__ void __launch_bounds__(kThreads, 2)
         auto tile = [&](auto LAST_, int it) -> bool {
             constexpr bool LAST = decltype(LAST_)::value;
             const int stage = it % kStages;
-            // bf16: V of this tile, P of head 0 and K of the next tile, checked
-            // together first; the bounded waits below only when one is missing
+            // V of this tile, P of head 0 and K of the next tile (Q8: its staged
+            // codes), checked together first; the bounded waits below only when
+            // one is missing
             bool ready = false;
-            if constexpr (!FP8) {
+            {
                 const int kn = LAST ? it : it + 1;
+                uint64_t *kb = Q8 ? &sm.st_full[kn % kStaged] : &sm.k_full[kn % kStages];
+                const uint32_t kp = Q8 ? (kn / kStaged) & 1 : (kn / kStages) & 1;
                 ready = mbar_try_wait3(&sm.v_full[stage], (it / kStages) & 1, &sm.p_full[0][stage], (it / kStages) & 1,
-                                       &sm.k_full[kn % kStages], (kn / kStages) & 1);
+                                       kb, kp);
             }
             if (!ready && !mbar_wait(&sm.v_full[stage], (it / kStages) & 1, p.status))
                 return false;
@@ -419,8 +422,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                 if (lane == 0)
                     issue_pv(t, stage, it > 0);
                 if constexpr (!LAST) {
-                    // (bf16: after head 0 the next K is known to be there)
-                    const bool k_known = !FP8 && (ready || t > 0);
+                    // (after head 0 the next K is known to be there)
+                    const bool k_known = ready || t > 0;
                     if (!k_known && !wait_k(it + 1))
                         return false;
                     tc_fence_after();
