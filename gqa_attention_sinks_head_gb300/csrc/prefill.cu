@@ -419,8 +419,11 @@ __global__ void __launch_bounds__(kThreads, 2)
                 if (!(ready && t == 0) && !mbar_wait(&sm.p_full[t][stage], (it / kStages) & 1, p.status))
                     return false;
                 tc_fence_after();
-                if (lane == 0)
+                if (lane == 0) {
                     issue_pv(t, stage, it > 0);
+                    if constexpr (LAST)
+                        umma_commit(&sm.o_done[t]);  // this head's O is final
+                }
                 if constexpr (!LAST) {
                     // (after head 0 the next K is known to be there)
                     const bool k_known = ready || t > 0;
@@ -447,7 +450,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             ok = tile(std::false_type{}, it);
         if (ok && ntiles > 0)
             ok = tile(std::true_type{}, ntiles - 1);
-        if (lane == 0)
+        if ((!ok || ntiles == 0) && lane == 0)  // (gave up: release the epilogues, which then see the status)
             for (int t = 0; t < NH; ++t)
                 umma_commit(&sm.o_done[t]);
         __syncwarp();
