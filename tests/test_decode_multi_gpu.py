@@ -53,6 +53,17 @@ def test_tokens_windows_splits(sa, oracle, q_len, window, splits):
 
 
 @pytest.mark.parametrize("q_len", [2, 4, 8])
+def test_tile_counts_one_to_six(sa, oracle, q_len):
+    """Unsplit blocks of 1 to 6 key tiles of 64, whole or with a partial last
+    tile: every shape of the MMA warp's round schedule (the steady rounds, the
+    two closing rounds without a next Q K^T, the last tile's zeroed rows past
+    the sequence, which the poisoned pages would otherwise turn into NaN)."""
+    lens = [64, 65, 128, 129, 192, 193, 256, 257, 320, 383]
+    case = case_of(q_len, lens, seed=430 + q_len, poison_pages=9)
+    run(sa, oracle, case, q_len, "q_len=%d tiles 1-6" % q_len, num_splits=1)
+
+
+@pytest.mark.parametrize("q_len", [2, 4, 8])
 @pytest.mark.parametrize("window", [1, 37])
 def test_small_windows(sa, oracle, q_len, window):
     # windows shorter than the token span: each token sees its own slice
