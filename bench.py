@@ -200,6 +200,55 @@ def timed_loop(torch, stream, one, steps, warmup, flush=None):
     return statistics.median(e0.elapsed_time(e1) for e0, e1 in evs)
 
 
+def timed_pipelined(torch, stream, ins, outs, calls, steps, warmup):
+    """Device time (ms) per step of a loop that overlaps each step's host
+    transfers with its neighbours' work, as a serving loop does: ins[b] /
+    outs[b] (b = step % 2) are Packed input / result buffers, and calls(b)
+    queues the step's library calls on `stream`, reading ins[b] and writing
+    outs[b].  Step k's inputs go up on an upload stream once step k - 2 no
+    longer reads that buffer; its results come back on a download stream once
+    they are written, while step k + 1 computes.  Every step still moves all
+    of its bytes.  Events on `stream` at the two ends of the K steps (the
+    last download included) time them; the result is their mean."""
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    in_free = [torch.cuda.Event() for _ in range(2)]
+    in_ready = [torch.cuda.Event() for _ in range(2)]
+    out_ready = [torch.cuda.Event() for _ in range(2)]
+    out_free = [torch.cuda.Event() for _ in range(2)]
+
+    def run(n):
+        for k in range(n):
+            b = k % 2
+            up.wait_event(in_free[b])
+            with torch.cuda.stream(up):
+                ins[b].h2d()
+            in_ready[b].record(up)
+            stream.wait_event(in_ready[b])
+            stream.wait_event(out_free[b])
+            calls(b)
+            in_free[b].record(stream)
+            out_ready[b].record(stream)
+            down.wait_event(out_ready[b])
+            with torch.cuda.stream(down):
+                outs[b].d2h()
+            out_free[b].record(down)
+
+    with torch.cuda.stream(stream):
+        for e in in_free + out_free:  # every wait below refers to a recorded event
+            e.record(stream)
+        run(warmup)
+        torch.cuda.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        up.wait_event(t0)
+        down.wait_event(t0)
+        run(steps)
+        stream.wait_event(out_free[(steps - 1) % 2])
+        t1.record(stream)
+        torch.cuda.synchronize()
+    return t0.elapsed_time(t1) / steps
+
+
 class Packed:
     """Tensors of one step laid out back to back (256-byte aligned) in one
     device buffer with a pinned host mirror, so that one copy moves them all:
@@ -329,7 +378,9 @@ class DecodeBench:
         self.kernels_per_step = sum(2 if cl["S"] > 1 else 1 for cl in self.calls)
         self.unit = "GB/s"
         self.dtype_name = "bf16" if self.elem == 2 else "fp8-e4m3 kv, bf16 q/out"
-        self.e2e_api = "sa_decode with pinned host q/seqlens/page table in, out/lse back; KV cache resident"
+        self.e2e_api = ("sa_decode with pinned host q/seqlens/page table in, out/lse back; KV cache resident; "
+                        "double-buffered (a step's copies overlap its neighbours' calls, steps back to back) "
+                        "unless the step needs an L2 flush")
 
     def amount(self):
         return self.step_bytes / 1e9
@@ -405,26 +456,34 @@ class DecodeBench:
     # ---- end to end through sa_decode with host buffers
     def e2e(self, stream, steps, warmup, flush=None):
         """Per step: one copy of q, the sequence lengths and the page table in,
-        the calls, one copy of every call's out and lse back."""
+        the calls, one copy of every call's out and lse back.  Double-buffered
+        (timed_pipelined) unless the step needs an L2 flush: then one step at
+        a time, its copies and calls in order on one stream."""
         import dataclasses
         torch = self.torch
         c = self.case
         paged = c.kv.page_table is not None
-        inp = Packed(torch, [c.q, c.seqlens] + ([c.kv.page_table] if paged else []))
-        q, seqlens = inp.dev[0], inp.dev[1]
-        kv = dataclasses.replace(c.kv, page_table=inp.dev[2]) if paged else c.kv
-        res = Packed(torch, [t for cl in self.calls for t in (cl["out"], cl["lse"])])
+        nbuf = 1 if flush is not None else 2
+        ins = [Packed(torch, [c.q, c.seqlens] + ([c.kv.page_table] if paged else [])) for _ in range(nbuf)]
+        outs = [Packed(torch, [t for cl in self.calls for t in (cl["out"], cl["lse"])]) for _ in range(nbuf)]
+        kvs = [dataclasses.replace(c.kv, page_table=inp.dev[2]) if paged else c.kv for inp in ins]
 
-        def one():
-            inp.h2d()
+        def calls(b):
             for i, cl in enumerate(self.calls):
-                self.sa.sa_decode(q, kv, seqlens, c.sinks, cl["window"], c.sm_scale, res.dev[2 * i],
-                                  res.dev[2 * i + 1], max_kv_len=self.maxlen, workspace=cl["ws"], num_splits=cl["S"],
-                                  stream=stream)
-            res.d2h()
+                self.sa.sa_decode(ins[b].dev[0], kvs[b], ins[b].dev[1], c.sinks, cl["window"], c.sm_scale,
+                                  outs[b].dev[2 * i], outs[b].dev[2 * i + 1], max_kv_len=self.maxlen,
+                                  workspace=cl["ws"], num_splits=cl["S"], stream=stream)
 
-        ms = timed_loop(torch, stream, one, steps, warmup, flush)
-        return ms, inp.nbytes, res.nbytes
+        if flush is None:
+            ms = timed_pipelined(torch, stream, ins, outs, calls, steps, warmup)
+        else:
+            def one():
+                ins[0].h2d()
+                calls(0)
+                outs[0].d2h()
+
+            ms = timed_loop(torch, stream, one, steps, warmup, flush)
+        return ms, ins[0].nbytes, outs[0].nbytes
 
     # ---- oracle on a bounded sample
     def oracle_sample(self, budget_s, max_seqs=None):
@@ -488,7 +547,8 @@ class MultiDecodeBench:
         self.unit = "GB/s"
         self.dtype_name = "bf16" if self.elem == 2 else "fp8-e4m3 kv, bf16 q/out"
         self.e2e_api = ("sa_decode_multi with pinned host q/seqlens/page table in, out/lse back; "
-                        "KV cache resident")
+                        "KV cache resident; double-buffered (a step's copies overlap its neighbours' calls, "
+                        "steps back to back)")
 
     def amount(self):
         return self.step_bytes / 1e9
@@ -535,21 +595,28 @@ class MultiDecodeBench:
         import dataclasses
         torch = self.torch
         c = self.case
-        inp = Packed(torch, [c.q, c.seqlens, c.kv.page_table])
-        q, seqlens = inp.dev[0], inp.dev[1]
-        kv = dataclasses.replace(c.kv, page_table=inp.dev[2])
-        res = Packed(torch, [t for cl in self.calls for t in (cl["out"], cl["lse"])])
+        nbuf = 1 if flush is not None else 2
+        ins = [Packed(torch, [c.q, c.seqlens, c.kv.page_table]) for _ in range(nbuf)]
+        outs = [Packed(torch, [t for cl in self.calls for t in (cl["out"], cl["lse"])]) for _ in range(nbuf)]
+        kvs = [dataclasses.replace(c.kv, page_table=inp.dev[2]) for inp in ins]
 
-        def one():
-            inp.h2d()
+        def calls(b):
             for i, cl in enumerate(self.calls):
-                self.sa.sa_decode_multi(q, self.q_len, kv, seqlens, c.sinks, cl["window"], c.sm_scale,
-                                        res.dev[2 * i], res.dev[2 * i + 1], max_kv_len=self.maxlen,
-                                        workspace=cl["ws"], num_splits=cl["S"], stream=stream)
-            res.d2h()
+                self.sa.sa_decode_multi(ins[b].dev[0], self.q_len, kvs[b], ins[b].dev[1], c.sinks, cl["window"],
+                                        c.sm_scale, outs[b].dev[2 * i], outs[b].dev[2 * i + 1],
+                                        max_kv_len=self.maxlen, workspace=cl["ws"], num_splits=cl["S"],
+                                        stream=stream)
 
-        ms = timed_loop(torch, stream, one, steps, warmup, flush)
-        return ms, inp.nbytes, res.nbytes
+        if flush is None:
+            ms = timed_pipelined(torch, stream, ins, outs, calls, steps, warmup)
+        else:
+            def one():
+                ins[0].h2d()
+                calls(0)
+                outs[0].d2h()
+
+            ms = timed_loop(torch, stream, one, steps, warmup, flush)
+        return ms, ins[0].nbytes, outs[0].nbytes
 
     def oracle_sample(self, budget_s, max_seqs=None):
         """Every token row of the first n sequences, all heads, every call."""
