@@ -146,6 +146,35 @@ __device__ __forceinline__ void widen_tile(const uint8_t *src, uint8_t *dst, int
     }
 }
 
+// One thread's 16-byte chunk of a key tile, placed once: its row, the chunk's
+// offset among the E4M3 codes (64-byte swizzle) and the offsets of its two
+// f16 halves in the widened tile (128-byte swizzle).  With NH = 2 the 256
+// softmax threads cover a tile's 256 chunks, one each.
+struct WidenPlan {
+    int r;
+    uint32_t src, lo, hi;
+};
+__device__ __forceinline__ WidenPlan widen_plan(int i)
+{
+    const int r = i >> 2, c = i & 3;
+    return WidenPlan{r, static_cast<uint32_t>(r * 64 + ((c ^ ((r >> 1) & 3)) << 4)),
+                     static_cast<uint32_t>(r * 128 + (((2 * c) ^ (r & 7)) << 4)),
+                     static_cast<uint32_t>(r * 128 + (((2 * c + 1) ^ (r & 7)) << 4))};
+}
+__device__ __forceinline__ void widen_chunk(const uint8_t *src, uint8_t *dst, const WidenPlan &w, int valid)
+{
+    uint4 x = make_uint4(0u, 0u, 0u, 0u);
+    if (w.r < valid)
+        x = *reinterpret_cast<const uint4 *>(src + w.src);
+    uint4 lo, hi;
+    e4m3x4_to_f16x2x2(x.x, lo.x, lo.y);
+    e4m3x4_to_f16x2x2(x.y, lo.z, lo.w);
+    e4m3x4_to_f16x2x2(x.z, hi.x, hi.y);
+    e4m3x4_to_f16x2x2(x.w, hi.z, hi.w);
+    *reinterpret_cast<uint4 *>(dst + w.lo) = lo;
+    *reinterpret_cast<uint4 *>(dst + w.hi) = hi;
+}
+
 __device__ __forceinline__ void kv_coords(const PrefillParams &p, int slot, int g, int page, int &c1, int &c2,
                                           int &c3)
 {
@@ -494,6 +523,9 @@ __global__ void __launch_bounds__(kThreads, 2)
                     mbar_arrive(&sm.q_conv);
             }
         }
+        // (the E4M3-query kernel keeps its scores in registers and has none to spare)
+        const WidenPlan wplan = (FP8 && !Q8 && NH == 2) ? widen_plan(static_cast<int>(threadIdx.x) - 32 * kFirstSoftmaxWarp)
+                                                        : WidenPlan{0, 0u, 0u, 0u};
         // FP8: widen the staged codes of tile j (K unless Q8, and V) into ring
         // stage j % kStages, this thread's share of the block's softmax threads
         auto widen = [&](int j) -> bool {
@@ -505,10 +537,16 @@ __global__ void __launch_bounds__(kThreads, 2)
             if (j >= kStages && !mbar_wait(&sm.kv_empty[stage], ((j / kStages) - 1) & 1, p.status))
                 return false;
             const int valid = min(BN, Lkv - (j_first + j) * BN);
-            const int wtid = static_cast<int>(threadIdx.x) - 32 * kFirstSoftmaxWarp;
-            if (!Q8)  // (Q8: the QK products read the key codes where TMA put them)
-                widen_tile(sm.k8[sb], sm.k[stage], valid, wtid, 128 * NH);
-            widen_tile(sm.v8[sb], sm.v[stage], valid, wtid, 128 * NH);
+            if constexpr (NH == 2 && !Q8) {
+                // one chunk of K and one of V per thread, at the offsets placed once
+                widen_chunk(sm.k8[sb], sm.k[stage], wplan, valid);
+                widen_chunk(sm.v8[sb], sm.v[stage], wplan, valid);
+            } else {
+                const int wtid = static_cast<int>(threadIdx.x) - 32 * kFirstSoftmaxWarp;
+                if (!Q8)  // (Q8: the QK products read the key codes where TMA put them)
+                    widen_tile(sm.k8[sb], sm.k[stage], valid, wtid, 128 * NH);
+                widen_tile(sm.v8[sb], sm.v[stage], valid, wtid, 128 * NH);
+            }
             fence_proxy_async_smem();  // generic writes -> tensor-core reads; staging reads -> next TMA
             __syncwarp();
             if (lane == 0) {
